@@ -1,0 +1,348 @@
+"""Benchmark of the routing-and-combine step of a decode-step latent-MoE layer.
+
+One step = router logits -> sigmoid+bias top-16 -> routing lists -> MXFP8 of the
+latent -> Finalize, on the wide decode batch (T = 1020 tokens = 204 requests x 5
+speculative tokens, hidden 7168, latent 3584, 896 experts, top-16), seeded synthetic
+inputs resident in HBM. Metric: tokens per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own replica of the
+step on its own GPU (the path shards by token: no data-path collective); value is the
+tokens of all ranks over the slowest rank's time. ``--impl reference`` times the CPU
+oracle (the plain C reference) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+T_WIDE = 1020
+WORKLOAD = "wide decode step: T=1020 tokens (204 requests x 5 speculative), hidden 7168, latent 3584, 896 experts, top-16"
+METRIC = "route+finalize tokens/s at T=1020 (1 GB300)"
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def algorithmic_bytes(T, H=synth.H, L=synth.L, E=synth.E, K=synth.K):
+    """Bytes each step must move (inputs read once, outputs written once)."""
+    return {
+        "router": T * H * 2 + E * H * 2 + T * E * 4,
+        "topk": T * E * 4 + E * 4 + T * K * (4 + 4 + 2),
+        "lists": T * K * 4 + (E + 1) * 4 + T * K * 4,
+        "mxfp8": T * L * 2 + T * L + T * L // 32,
+        "finalize": T * K * L * 2 + T * K * 2 + T * L * 2,
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel's
+    source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(name)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "latent_moe_decode_gb300", "csrc", d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha256_16"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def __enter__(self):
+        try:
+            import tempfile
+
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200", "-i", str(self.index)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if not self.proc or not self.path:
+            return None
+        rows = []
+        for line in open(self.path):
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[3:7]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        mx = max(r[1] for r in rows)
+        load = [r[0] for r in rows] or [0.0]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    m.load()
+    T = T_WIDE
+    d = synth.chain_inputs(T, seed=rank)
+    tob = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    x, w, latent, rows = tob(d["x"]), tob(d["w"]), tob(d["latent"]), tob(d["rows"])
+    bias = torch.from_numpy(d["bias"]).to(dev)
+    rf = m.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        rf.run(x, w, bias, latent, rows)
+    barrier()
+
+    # (a) the chain, L2 flushed before every step (outside the step's events)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            rf.run(x, w, bias, latent, rows)
+            ev[i][1].record(stream)
+        barrier()
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+
+        # (b) each call alone (cold L2) for the per-kernel roofline
+        calls = {
+            "router": lambda: m.router_logits(x, w, out=rf.logits, workspace=rf.router_ws),
+            "topk": lambda: m.topk_route(rf.logits, bias, synth.K, ids=rf.ids, weights=rf.weights, weights_bf16=rf.weights_bf16),
+            "lists": lambda: m.build_routing_lists(rf.ids, synth.E, offsets=rf.offsets, pairs=rf.pairs, workspace=rf.lists_ws),
+            "mxfp8": lambda: m.mxfp8_quantize_rows(latent, q=rf.q, scales=rf.scales),
+            "finalize": lambda: m.finalize(rows, rf.weights_bf16, T, synth.K, out=rf.out),
+        }
+        per = {k: [] for k in calls}
+        for i in range(args.steps):
+            for k, fn in calls.items():
+                flush.fill_(i & 0xFF)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                per[k].append((a, b))
+        barrier()
+        per_ms = {k: float(np.mean([a.elapsed_time(b) for a, b in v])) for k, v in per.items()}
+    clocks = clk.summary()
+    assert m.device_error(clear=True) == 0
+
+    # (c) end to end through the public API: pinned host inputs in, results out
+    hx = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(d["latent"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hr = torch.from_numpy(d["rows"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    outs = [rf.out, rf.ids, rf.weights_bf16, rf.offsets, rf.pairs, rf.q, rf.scales]
+    houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hl, hr))
+    d2h = sum(t.numel() * t.element_size() for t in houts)
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        latent.copy_(hl, non_blocking=True)
+        rows.copy_(hr, non_blocking=True)
+        rf.run(x, w, bias, latent, rows)
+        for h, o in zip(houts, outs):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        e_ev[i][0].record(stream)
+        e2e_step()
+        e_ev[i][1].record(stream)
+    barrier()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
+
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    ab = algorithmic_bytes(T)
+    fin_gbs = ab["finalize"] / (per_ms["finalize"] * 1e-3) / 1e9
+    traffic = kernel_traffic("finalize")
+    steps = {}
+    for k in calls:
+        gbs = ab[k] / (per_ms[k] * 1e-3) / 1e9
+        steps[k] = {"us": round(per_ms[k] * 1e3, 2), "alg_bytes": ab[k], "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    flops = 2.0 * T * synth.E * synth.H
+    steps["router"]["TFLOP/s"] = round(flops / (per_ms["router"] * 1e-3) / 1e12, 1)
+    steps["router"]["frac_bf16"] = round(flops / (per_ms["router"] * 1e-3) / 1e12 / bf16, 3)
+    line = {
+        "metric": METRIC,
+        "value": round(world * T / (ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the pages' wide decode batch)",
+        "config": {"workload": WORKLOAD, "T": T, "hidden": synth.H, "latent": synth.L, "experts": synth.E, "top_k": synth.K,
+                   "l2": "flushed (256 MB write) before every timed step, outside its events",
+                   "parallelism": f"replicas x{world} (token-sharded, no collective)"},
+        "chain_GB/s": round(sum(ab.values()) / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"kernel": "finalize", "bound": "hbm", "achieved": round(fin_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(fin_gbs / hbm, 3), "traffic": traffic, "alg_bytes_per_launch": ab["finalize"],
+                     "peak_source": f"{peak_src} (copy bandwidth, MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"},
+        "steps_alone": steps,
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * rf.launches,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------------------
+def oracle_step(d, tokens):
+    """The oracle's whole step over the given token rows of the wide batch."""
+    import oracle
+
+    x = d["x"][tokens]
+    logits, _ = oracle.router_logits(x, d["w"])
+    ids, wf, wb = oracle.topk_route(logits.astype(np.float32), d["bias"], synth.K)
+    oracle.routing_lists(ids, synth.E)
+    oracle.mxfp8_quantize(d["latent"][tokens])
+    rows = d["rows"].reshape(T_WIDE, synth.K, synth.L)[tokens].reshape(-1, synth.L)
+    oracle.finalize(rows, wb, len(tokens), synth.K)
+
+
+def cpu_baseline(seconds):
+    """The oracle as it stands, single-threaded on a host core, on consecutive 16-token
+    slices of the wide batch until about `seconds` of CPU work."""
+    import oracle
+
+    oracle.build()
+    d = synth.chain_inputs(T_WIDE)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds and n < T_WIDE:
+        oracle_step(d, np.arange(n, min(n + 16, T_WIDE)))
+        n = min(n + 16, T_WIDE)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of the {T_WIDE} tokens of the wide batch, whole step, {dt:.1f} s"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    tot = 0.0
+    for _ in range(args.warmup):
+        pass  # the oracle has no caches to warm beyond its first call below
+    base = cpu_baseline(max(2.0, args.cpu_seconds / max(1, args.steps)) * args.steps)
+    v = base["value"]
+    tot = T_WIDE / v
+    return {
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 router / f32 rest", "data": "synthetic (seeded)", "impl": "reference",
+        "config": {"workload": WORKLOAD, "T": T_WIDE},
+        "cpu_baseline": base,
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 (sm_103a) routing-and-combine path of a
+ * decode-step latent-MoE layer.
+ *
+ * The path, per decode step of T token rows:
+ *   router logits (BF16 x, BF16 gate -> FP32)  ->  sigmoid + bias top-k with
+ *   renormalised weights  ->  per-expert routing lists  ||  MXFP8 quantisation of the
+ *   latent rows  ->  Finalize (the weighted top-k sum of the experts' rows).
+ *
+ * Source pages (vLLM API documentation):
+ *   [wide] "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide"
+ *   [ep]   "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.layer"
+ *   [fin]  "vllm.models.glm5next.nvidia.specialized_decode.cutedsl.finalize_publish"
+ *
+ * Conventions shared by every call
+ *   - Pointers named as device buffers must be device (or managed) memory of the
+ *     current CUDA device; the caller owns every buffer. The library never allocates,
+ *     frees or synchronises in these calls, and keeps no per-call state.
+ *   - Every call is asynchronous and stream ordered on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream). Kernels are launched with programmatic
+ *     dependent launch, so consecutive calls on one stream overlap their launch
+ *     latency; each kernel waits for its predecessor before touching dependent data.
+ *   - Arguments are validated synchronously before anything is launched; on an
+ *     error nothing is launched and the status says why. No exception crosses the ABI.
+ *   - BF16 tensors are passed as uint16_t bit patterns, E4M3 / E8M0 bytes as uint8_t.
+ *     Tensors are dense row-major.
+ *   - Data-dependent errors that only the GPU can see (an out-of-range index) do not
+ *     fault: the kernel skips the offending element and sets a bit in the library's
+ *     device error word, read with moe_device_error().
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (identical to cudaStream_t / CUstream). */
+typedef struct CUstream_st* moe_stream_t;
+
+/* Status codes returned by every call. */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARGUMENT 1 /* bad size, null required pointer, bad flag (the pages' ValueError on a bad width) */
+#define MOE_ERR_ALIGNMENT 2        /* a vectorised pointer is not 16-byte aligned */
+#define MOE_ERR_CAPACITY 3         /* a size beyond what the call supports (the pages' ValueError on tokens outside capacity) */
+#define MOE_ERR_WORKSPACE 4        /* workspace missing or smaller than the *_workspace() query (the pages' RuntimeError on scratch misuse) */
+#define MOE_ERR_UNSUPPORTED 5      /* no GPU, or a device that is not sm_103 */
+#define MOE_ERR_CUDA 6             /* a CUDA runtime/driver call or a launch failed */
+
+/* Bits of the device error word (see moe_device_error). */
+#define MOE_DEVERR_ROW_INDEX 0x1u /* moe_finalize: a row index outside [-1, n_rows); that term was skipped */
+#define MOE_DEVERR_EXPERT_ID 0x2u /* moe_build_routing_lists: an expert id outside [0, E); that pair was dropped */
+#define MOE_DEVERR_TIMEOUT 0x4u   /* a bounded wait inside a kernel gave up; that kernel's output is invalid */
+
+/* Weight dtypes for moe_finalize. */
+#define MOE_DTYPE_F32 0
+#define MOE_DTYPE_BF16 1
+
+/* Limits. */
+#define MOE_MAX_EXPERTS 1024 /* E of moe_topk_route and moe_build_routing_lists */
+#define MOE_MAX_TOPK 32      /* K of every call */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int moe_version(void);
+
+/*
+ * Read the device error word of the current device into *bits (may be NULL) and, if
+ * clear != 0, reset it to zero. Synchronous: waits for all work on the device.
+ * Returns MOE_OK or MOE_ERR_CUDA / MOE_ERR_UNSUPPORTED.
+ */
+int moe_device_error(uint32_t* bits, int clear);
+
+/* -------------------------------------------------------------------------------
+ * Router logits.
+ *   logits[t, e] = sum_j x[t, j] * w[e, j]      (FP32 accumulate and output, no bias)
+ * Source: [ep] EpMoeLayer.stock_order (mm(x, gate^T) with an FP32 output) and
+ * EpMoeLayer.__init__ (the FP32-output split-K router projection, "split-K reduces in
+ * FP32", module docstring); [wide] module docstring ("FP32 router logits").
+ *
+ *   x         device, BF16 [T, H]        hidden rows
+ *   w         device, BF16 [E, H]        router weight (gate), expert rows
+ *   logits    device, FP32 [T, E]        output
+ *   workspace device scratch of at least moe_router_logits_workspace(T, H, E) bytes
+ *             (may be NULL when that query returns 0); its contents on entry do not
+ *             matter and are clobbered. Calls that share a workspace must not overlap.
+ * Requirements: T >= 1, E >= 1, H >= 8, H % 8 == 0; x, w 16-byte aligned
+ * (MOE_ERR_ALIGNMENT), logits 4-byte aligned.
+ * Numerics: BF16 products are exact in FP32; sums are accumulated in FP32 on the tensor
+ * cores in K-chunks, the split-K partials reduced in a fixed order, so the result is
+ * deterministic run to run. The error is well inside 1e-5 * sum_j |x[t,j] w[e,j]|.
+ * ------------------------------------------------------------------------------- */
+size_t moe_router_logits_workspace(int T, int H, int E);
+int moe_router_logits(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E,
+                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* The same computation with an explicit kernel family: MOE_ROUTER_AUTO (what
+ * moe_router_logits uses), MOE_ROUTER_SIMT (CUDA-core split-K, per-lane FP32 chains of
+ * at most 128 products, then a fixed butterfly) or MOE_ROUTER_TCGEN05 (tensor-core
+ * split-K with a TMEM accumulator). The workspace query covers every family. */
+#define MOE_ROUTER_AUTO 0
+#define MOE_ROUTER_SIMT 1
+#define MOE_ROUTER_TCGEN05 2
+int moe_router_logits_ex(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E,
+                         void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
+ * Sigmoid + e_score_correction_bias top-K with renormalised weights.
+ * Source: [ep] EpMoeLayer.topk (one group, sigmoid scoring, correction bias,
+ * renormalize, routed scaling); [wide] WideRoute docstring ("exact top16 and
+ * renormalized weights"); [wide] WideMoE.__init__ (bias, renorm, scale taken from the
+ * module); [wide] WideScratch (ids int32 [cap, 16], weights BF16 [cap, 16]).
+ *
+ * Per token t:
+ *   s_e = sigmoid(logits[t, e])  (the library's specified sigmoid: exp by Cody-Waite
+ *         reduction + degree-7 Taylor, FP32 add, correctly rounded division;
+ *         s = 1 for x >= 17.5, s = 0 for x <= -88.5)
+ *   c_e = s_e + bias[e]          (c_e = s_e when bias is NULL)
+ *   ids[t, k]  = the k-th expert in the order (c descending, expert index ascending)
+ *   S          = s_{ids[t,0]} + ... + s_{ids[t,K-1]}   (FP32, slot order)
+ *   weights[t, k] = renormalize ? (S == 0 ? 0 : s_{ids[t,k]} / S) : s_{ids[t,k]},
+ *                   then times `scale` when scale != 1
+ *   weights_bf16[t, k] = weights[t, k] rounded to nearest even BF16.
+ * Weights use the unbiased scores. NaN keys rank below every number.
+ *
+ *   logits       device, FP32 [T, E]
+ *   bias         device, FP32 [E] or NULL
+ *   ids          device, int32 [T, K]   output
+ *   weights      device, FP32 [T, K]    output (may be NULL)
+ *   weights_bf16 device, BF16 [T, K]    output (may be NULL)
+ * Requirements: T >= 1, 1 <= K <= min(E, MOE_MAX_TOPK), 1 <= E <= MOE_MAX_EXPERTS
+ * (MOE_ERR_CAPACITY beyond), logits 16-byte aligned when E % 4 == 0.
+ * Bit-exact and deterministic.
+ * ------------------------------------------------------------------------------- */
+int moe_topk_route(const float* logits, const float* bias, int T, int E, int K, int renormalize,
+                   float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,
+                   moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
+ * Per-expert routing lists (counting sort, CSR).
+ * Source: [wide] WideRoute docstring and kernel: each of token t's K (token, slot)
+ * pairs is appended to its expert's list as the pair code t*K + k, which is also the
+ * expanded-row index that Finalize reads.
+ *
+ *   pairs[offsets[e] .. offsets[e+1]) = the codes t*K + k with ids[t, k] == e, in
+ *   ascending t (so ascending code). offsets = exclusive prefix sum of the per-expert
+ *   counts; offsets[0] = 0, offsets[E] = T*K.
+ *
+ *   ids       device, int32 [T, K]   (within a row the ids must be distinct)
+ *   offsets   device, int32 [E + 1]  output
+ *   pairs     device, int32 [T * K]  output
+ *   workspace device scratch of moe_build_routing_lists_workspace(T, K, E) bytes (0 for
+ *             T <= 1024: then NULL is fine); clobbered.
+ * Requirements: T >= 0 (T == 0 writes offsets = 0), 1 <= K <= MOE_MAX_TOPK,
+ * 1 <= E <= MOE_MAX_EXPERTS, ids 16-byte aligned when K % 4 == 0.
+ * An id outside [0, E) is dropped and sets MOE_DEVERR_EXPERT_ID (the lists are then
+ * incomplete). Deterministic and free of global atomics.
+ * ------------------------------------------------------------------------------- */
+size_t moe_build_routing_lists_workspace(int T, int K, int E);
+int moe_build_routing_lists(const int32_t* ids, int T, int K, int E, int32_t* offsets,
+                            int32_t* pairs, void* workspace, size_t workspace_bytes,
+                            moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
+ * MXFP8 (OCP Microscaling) quantisation of BF16 rows.
+ * Source: [wide] module docstring ("MXFP8 activations") and WideRoute (the token's
+ * MXFP8 plan row written from its BF16 latent); [ep] module docstring ("the MXFP8
+ * latent"). Read as OCP MX v1.0: per block of 32 consecutive elements of a row,
+ *   se = clamp(floor(log2(max |v|)) - 8, -127, 127),   scale byte = se + 127 (E8M0),
+ *   q  = E4M3(v * 2^-se), round to nearest even, saturating to +-448, sign kept.
+ * An all-zero block has scale byte 0 and signed-zero elements; a block holding an
+ * infinity or NaN has scale byte 0xFF and elements 0x7F.
+ *
+ *   x       device, BF16 [rows, cols]
+ *   q       device, E4M3 bytes [rows, cols]      output
+ *   scales  device, E8M0 bytes [rows, cols/32]   output, row-major
+ * Requirements: rows >= 0, cols >= 32, cols % 32 == 0; x 16-byte aligned, q and scales
+ * 8-byte aligned. Bit-exact.
+ * ------------------------------------------------------------------------------- */
+int mxfp8_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
+                        moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
+ * Finalize: the routing-weighted top-K sum, optionally with the shared expert.
+ * Source: [wide] Finalize (out[t] = sum_k w[t,k] * rows[16t + k], FP32, k in order,
+ * fma, one BF16 rounding; all of a thread's row loads in flight before the math);
+ * [fin] _QuadFinalizePublishDeviceKernel (weights read as BF16 or FP32, times
+ * routed_scaling_factor when it is not 1, zero for a -1 permuted index whose row is
+ * skipped, the shared-expert row added once in FP32 after all k, then one rounding).
+ *
+ * Per token t and column c, with r(t,k) = row_index ? row_index[t*K+k] : t*K + k:
+ *   w_k  = float(weights[t,k]); if scale != 1: w_k = w_k * scale
+ *   acc  = +0; for k = 0..K-1 in order: if r(t,k) != -1: acc = fma(w_k, rows[r(t,k), c], acc)
+ *   if shared: acc = acc + shared[t, c]
+ *   out[t, c] = bf16_rne(acc)
+ *
+ *   rows       device, BF16 [n_rows, H]
+ *   row_index  device, int32 [T, K] or NULL (then row t*K + k; n_rows >= T*K required)
+ *   weights    device, [T, K] FP32 (weights_dtype MOE_DTYPE_F32) or BF16 (MOE_DTYPE_BF16)
+ *   shared     device, BF16 [T, H] or NULL
+ *   out        device, BF16 [T, H]   output (must not alias the inputs)
+ * Requirements: T >= 0, 1 <= K <= MOE_MAX_TOPK, H >= 8, H % 8 == 0; rows, shared, out
+ * 16-byte aligned. An index outside [-1, n_rows) skips its term and sets
+ * MOE_DEVERR_ROW_INDEX. Bit-exact and deterministic.
+ * ------------------------------------------------------------------------------- */
+int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index,
+                 const void* weights, int weights_dtype, const uint16_t* shared,
+                 float routed_scaling_factor, int T, int K, int H, uint16_t* out,
+                 moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

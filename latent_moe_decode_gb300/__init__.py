@@ -1,0 +1,247 @@
+"""GB300 (sm_103a) routing-and-combine path of a decode-step latent-MoE layer.
+
+A thin ctypes binding over ``libmoe_decode.so`` (C ABI in ``include/moe_decode.h``):
+it checks torch tensors (device, dtype, shape, contiguity), passes their device
+pointers and the current CUDA stream, and turns status codes into exceptions. Every
+step of the path runs in the library's CUDA kernels; there is no fallback.
+
+BF16 tensors are ``torch.bfloat16``; E4M3 / E8M0 outputs are ``torch.uint8``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MoeError", "load", "router_logits", "router_logits_workspace", "topk_route",
+    "build_routing_lists", "build_routing_lists_workspace", "mxfp8_quantize_rows",
+    "finalize", "device_error", "RouteFinalize",
+    "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05",
+    "DEVERR_ROW_INDEX", "DEVERR_EXPERT_ID", "DEVERR_TIMEOUT",
+]
+
+OK, ERR_INVALID_ARGUMENT, ERR_ALIGNMENT, ERR_CAPACITY, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA = range(7)
+DEVERR_ROW_INDEX, DEVERR_EXPERT_ID, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+ROUTER_AUTO, ROUTER_SIMT, ROUTER_TCGEN05 = 0, 1, 2
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+# Every symbol the header declares, with its ctypes signature.
+_P, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_version": (_I, []),
+    "moe_device_error": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
+    "moe_router_logits_workspace": (_SZ, [_I, _I, _I]),
+    "moe_router_logits": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "moe_router_logits_ex": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _I, _P]),
+    "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "moe_build_routing_lists_workspace": (_SZ, [_I, _I, _I]),
+    "moe_build_routing_lists": (_I, [_P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
+    "moe_finalize": (_I, [_P, ctypes.c_int64, _P, _P, _I, _P, _F, _I, _I, _I, _P, _P]),
+}
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = load().moe_status_string(status).decode()
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (built in-tree by ``build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build the CUDA library first (latent_moe_decode_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise MoeError(fn, status)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, shape=None, name="tensor"):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ---------------------------------------------------------------------------
+def router_logits_workspace(T: int, H: int, E: int) -> int:
+    return int(load().moe_router_logits_workspace(T, H, E))
+
+
+def router_logits(x, w, out=None, workspace=None, algo: int = ROUTER_AUTO, stream=None):
+    """FP32 logits [T, E] = x [T, H] (BF16) @ w [E, H]^T (BF16)."""
+    T, H = x.shape
+    E = w.shape[0]
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(w, torch.bfloat16, (E, H), "w")
+    out = _empty((T, E), torch.float32, x) if out is None else _need(out, torch.float32, (T, E), "out")
+    need = router_logits_workspace(T, H, E)
+    if need and workspace is None:
+        workspace = _empty((need,), torch.uint8, x)
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_router_logits_ex", load().moe_router_logits_ex(
+        _ptr(x), _ptr(w), _ptr(out), T, H, E, _ptr(workspace), wb, algo, _stream(stream)))
+    return out
+
+
+def topk_route(logits, bias, K: int, renormalize: bool = True, scale: float = 1.0,
+               ids=None, weights=None, weights_bf16=None, want_bf16: bool = True, stream=None):
+    """(ids int32 [T,K], weights FP32 [T,K], weights BF16 [T,K] or None)."""
+    T, E = logits.shape
+    _need(logits, torch.float32, (T, E), "logits")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    ids = _empty((T, K), torch.int32, logits) if ids is None else _need(ids, torch.int32, (T, K), "ids")
+    weights = _empty((T, K), torch.float32, logits) if weights is None else _need(weights, torch.float32, (T, K), "weights")
+    if weights_bf16 is None and want_bf16:
+        weights_bf16 = _empty((T, K), torch.bfloat16, logits)
+    elif weights_bf16 is not None:
+        _need(weights_bf16, torch.bfloat16, (T, K), "weights_bf16")
+    _check("moe_topk_route", load().moe_topk_route(
+        _ptr(logits), _ptr(bias), T, E, K, int(bool(renormalize)), float(scale),
+        _ptr(ids), _ptr(weights), _ptr(weights_bf16), _stream(stream)))
+    return ids, weights, weights_bf16
+
+
+def build_routing_lists_workspace(T: int, K: int, E: int) -> int:
+    return int(load().moe_build_routing_lists_workspace(T, K, E))
+
+
+def build_routing_lists(ids, E: int, offsets=None, pairs=None, workspace=None, stream=None):
+    """CSR lists: offsets int32 [E+1], pairs int32 [T*K] (pair code t*K + k)."""
+    T, K = ids.shape
+    _need(ids, torch.int32, (T, K), "ids")
+    offsets = _empty((E + 1,), torch.int32, ids) if offsets is None else _need(offsets, torch.int32, (E + 1,), "offsets")
+    pairs = _empty((T * K,), torch.int32, ids) if pairs is None else _need(pairs, torch.int32, (T * K,), "pairs")
+    need = build_routing_lists_workspace(T, K, E)
+    if need and workspace is None:
+        workspace = _empty((need,), torch.uint8, ids)
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_build_routing_lists", load().moe_build_routing_lists(
+        _ptr(ids), T, K, E, _ptr(offsets), _ptr(pairs), _ptr(workspace), wb, _stream(stream)))
+    return offsets, pairs
+
+
+def mxfp8_quantize_rows(x, q=None, scales=None, stream=None):
+    """(E4M3 bytes uint8 [rows, cols], E8M0 scale bytes uint8 [rows, cols/32])."""
+    rows, cols = x.shape
+    _need(x, torch.bfloat16, (rows, cols), "x")
+    q = _empty((rows, cols), torch.uint8, x) if q is None else _need(q, torch.uint8, (rows, cols), "q")
+    nb = cols // 32
+    scales = _empty((rows, nb), torch.uint8, x) if scales is None else _need(scales, torch.uint8, (rows, nb), "scales")
+    _check("mxfp8_quantize_rows", load().mxfp8_quantize_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scales), _stream(stream)))
+    return q, scales
+
+
+def finalize(rows, weights, T: int, K: int, row_index=None, shared=None, scale: float = 1.0, out=None, stream=None):
+    """BF16 out [T, H] = sum_k w[t,k] * rows[r(t,k)] (+ shared[t])."""
+    n_rows, H = rows.shape
+    _need(rows, torch.bfloat16, (n_rows, H), "rows")
+    if weights.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif weights.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError("weights: expected float32 or bfloat16")
+    _need(weights, weights.dtype, (T, K), "weights")
+    if row_index is not None:
+        _need(row_index, torch.int32, (T, K), "row_index")
+    if shared is not None:
+        _need(shared, torch.bfloat16, (T, H), "shared")
+    out = _empty((T, H), torch.bfloat16, rows) if out is None else _need(out, torch.bfloat16, (T, H), "out")
+    _check("moe_finalize", load().moe_finalize(
+        _ptr(rows), n_rows, _ptr(row_index), _ptr(weights), dt, _ptr(shared), float(scale), T, K, H, _ptr(out),
+        _stream(stream)))
+    return out
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's device error word (DEVERR_* bits); synchronises the device."""
+    v = ctypes.c_uint32(0)
+    _check("moe_device_error", load().moe_device_error(ctypes.byref(v), int(bool(clear))))
+    return int(v.value)
+
+
+class RouteFinalize:
+    """The whole routing-and-combine step on one stream, with its buffers preallocated:
+    router logits -> sigmoid+bias top-K -> routing lists -> MXFP8 latent -> Finalize.
+
+    ``run()`` launches the library's kernels back to back (programmatic dependent
+    launch between them) and allocates nothing, so it can be captured in a CUDA graph.
+    """
+
+    def __init__(self, T: int, H: int, L: int, E: int, K: int, device="cuda", renormalize=True, scale=1.0,
+                 router_algo: int = ROUTER_AUTO):
+        self.T, self.H, self.L, self.E, self.K = T, H, L, E, K
+        self.renormalize, self.scale, self.router_algo = renormalize, scale, router_algo
+        dev = torch.device(device)
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        self.logits = e((T, E), torch.float32)
+        self.ids = e((T, K), torch.int32)
+        self.weights = e((T, K), torch.float32)
+        self.weights_bf16 = e((T, K), torch.bfloat16)
+        self.offsets = e((E + 1,), torch.int32)
+        self.pairs = e((T * K,), torch.int32)
+        self.q = e((T, L), torch.uint8)
+        self.scales = e((T, L // 32), torch.uint8)
+        self.out = e((T, L), torch.bfloat16)
+        self.router_ws = e((max(1, router_logits_workspace(T, H, E)),), torch.uint8)
+        self.lists_ws = e((max(1, build_routing_lists_workspace(T, K, E)),), torch.uint8)
+        self.launches = self._count_launches()
+
+    def _count_launches(self) -> int:
+        """Kernels one run() launches."""
+        # router (+ split-K reduce), top-k, lists (1 or 2), MXFP8, Finalize
+        return 5 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0) + (
+            1 if build_routing_lists_workspace(self.T, self.K, self.E) > 0 else 0)
+
+    def run(self, x, w, bias, latent, rows, stream=None):
+        router_logits(x, w, out=self.logits, workspace=self.router_ws, algo=self.router_algo, stream=stream)
+        topk_route(self.logits, bias, self.K, self.renormalize, self.scale, ids=self.ids, weights=self.weights,
+                   weights_bf16=self.weights_bf16, stream=stream)
+        build_routing_lists(self.ids, self.E, offsets=self.offsets, pairs=self.pairs, workspace=self.lists_ws,
+                            stream=stream)
+        mxfp8_quantize_rows(latent, q=self.q, scales=self.scales, stream=stream)
+        finalize(rows, self.weights_bf16, self.T, self.K, out=self.out, stream=stream)
+        return self.out

@@ -1,0 +1,123 @@
+// Router logits on the CUDA cores (small token counts) and the split-K reduce.
+//
+// Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.layer,
+// EpMoeLayer (the FP32-output split-K router projection of the [896, 7168] BF16 gate:
+// split 4 for up to 32 tokens, 64-row weight tiles, "split-K reduces in FP32") and
+// EpMoeLayer.stock_order (mm(x, gate^T) with an FP32 output).
+//
+// GB300 design: at a handful of tokens the router is one pass over the 12.8 MB weight,
+// HBM-bound on the CUDA cores. A CTA of 8 warps owns 16 experts (2 per warp) x 16
+// tokens x one K chunk; the chunk of the 16 hidden rows is staged in shared memory and
+// every lane streams 16-byte weight fragments (a warp reads 512 contiguous bytes of an
+// expert row per load). A lane accumulates <= 128 products per output in FP32, then the
+// 32 lane partials of the warp's 32 outputs are combined by a transposing butterfly
+// (31 shuffles), after which lane l holds output l. Split-K partials go to the
+// workspace and a second kernel sums them in split order (deterministic).
+#include "router.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* __restrict__ x,
+                                                               const uint16_t* __restrict__ w, float* __restrict__ out,
+                                                               int T, int H, int E, int kc) {
+  extern __shared__ uint4 xs[];  // [16 tokens][kc / 8]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.y * 16;
+  const int e0 = blockIdx.x * 16 + 2 * warp;
+  const int s = blockIdx.z;
+  const int kb = s * kc;
+  const int len8 = (min(H, kb + kc) - kb) / 8;
+  const int row8 = kc / 8;
+  grid_launch_dependents();
+  grid_wait();
+  for (int i = threadIdx.x; i < 16 * len8; i += kThreads) {
+    const int tt = i / len8, kk = i - tt * len8;
+    xs[tt * row8 + kk] = (t0 + tt < T) ? ld_nc16(x + (size_t)(t0 + tt) * H + kb + kk * 8) : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  const uint16_t* wa = w + (size_t)min(e0, E - 1) * H + kb;
+  const uint16_t* wb = w + (size_t)min(e0 + 1, E - 1) * H + kb;
+  for (int kk = lane; kk < len8; kk += 32) {
+    const uint4 va = ld_nc16(wa + kk * 8), vb = ld_nc16(wb + kk * 8);
+    const uint32_t a4[4] = {va.x, va.y, va.z, va.w}, b4[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      const uint4 xv = xs[tt * row8 + kk];
+      const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[tt] = __fmaf_rn(bf16_lo(a4[j]), bf16_lo(x4[j]), acc[tt]);
+        acc[tt] = __fmaf_rn(bf16_hi(a4[j]), bf16_hi(x4[j]), acc[tt]);
+        acc[16 + tt] = __fmaf_rn(bf16_lo(b4[j]), bf16_lo(x4[j]), acc[16 + tt]);
+        acc[16 + tt] = __fmaf_rn(bf16_hi(b4[j]), bf16_hi(x4[j]), acc[16 + tt]);
+      }
+    }
+  }
+  // transposing butterfly: afterwards lane l holds the warp total of output l
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? acc[i] : acc[i + off];
+      const float keep = upper ? acc[i + off] : acc[i];
+      acc[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
+    }
+  }
+  const int e = e0 + (lane >> 4), t = t0 + (lane & 15);
+  if (e < E && t < T) out[((size_t)s * T + t) * E + e] = acc[0];
+}
+
+__global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ part, int S, long long n,
+                                                            float* __restrict__ logits) {
+  grid_launch_dependents();
+  grid_wait();
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
+    float v = part[i];
+    for (int s = 1; s < S; ++s) v = __fadd_rn(v, part[(size_t)s * n + i]);
+    logits[i] = v;
+  }
+}
+
+}  // namespace
+
+// Splits of the SIMT path: per-lane chains of at most 128 products (kc <= 4096) and
+// enough CTAs to cover the SMs twice.
+void simt_plan(int T, int H, int E, int sm_count, int* S, int* kc) {
+  const long long tiles = (long long)((E + 15) / 16) * ((T + 15) / 16);
+  int s = (int)((2LL * sm_count + tiles - 1) / tiles);
+  s = max(s, (H + 4095) / 4096);
+  s = min(s, max(1, H / 256));
+  int k = (H + s - 1) / s;
+  k = (k + 255) / 256 * 256;
+  *S = (H + k - 1) / k;
+  *kc = k;
+}
+
+int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int S, int kc,
+                       float* part, cudaStream_t stream) {
+  const size_t smem = (size_t)16 * kc * 2;
+  if (cudaFuncSetAttribute(router_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  dim3 grid((E + 15) / 16, (T + 15) / 16, S);
+  int st = launch_pdl(router_simt_kernel, grid, dim3(kThreads), smem, stream, x, w, S == 1 ? logits : part, T, H, E, kc);
+  if (st != MOE_OK || S == 1) return st;
+  return launch_router_reduce(part, S, T, E, logits, stream);
+}
+
+int launch_router_reduce(const float* part, int S, int T, int E, float* logits, cudaStream_t stream) {
+  const long long n = (long long)T * E;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  return launch_pdl(router_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, part, S, n, logits);
+}
+
+}  // namespace moe

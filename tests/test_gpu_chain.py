@@ -1,0 +1,79 @@
+"""The whole routing-and-combine step on one stream (router -> top-16 -> lists ||
+MXFP8 -> Finalize, programmatic dependent launches between the kernels) against the
+oracle, at the decode shapes: logits within tolerance, everything else bit for bit,
+with the oracle's top-k consuming the GPU's logits."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import bf16_bits, bf16_dev, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_chain(moe, orc, T, skew=False, samples=None, graph=False):
+    d = synth.chain_inputs(T, skew=skew)
+    x, w, bias, latent, rows = bf16_dev(d["x"]), bf16_dev(d["w"]), dev(d["bias"]), bf16_dev(d["latent"]), bf16_dev(d["rows"])
+    rf = moe.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K)
+    if graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            rf.run(x, w, bias, latent, rows)  # warm-up outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            rf.run(x, w, bias, latent, rows)
+        rf.out.zero_()
+        g.replay()
+    else:
+        rf.run(x, w, bias, latent, rows)
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 0
+    logits = host(rf.logits)
+    # R1 logits, sampled or full, against FP64
+    if samples:
+        rng = np.random.default_rng(T)
+        t, e = rng.integers(0, T, samples).astype(np.int32), rng.integers(0, synth.E, samples).astype(np.int32)
+        exp, ab = orc.router_logits_sampled(d["x"], d["w"], t, e)
+        assert np.all(np.abs(logits[t, e].astype(np.float64) - exp) <= 1e-5 * ab)
+    else:
+        exp, ab = orc.router_logits(d["x"], d["w"])
+        assert np.all(np.abs(logits.astype(np.float64) - exp) <= 1e-5 * ab)
+    # R2 top-16 from the GPU's logits
+    ids, wf, wb = orc.topk_route(logits, d["bias"], synth.K)
+    np.testing.assert_array_equal(host(rf.ids), ids)
+    np.testing.assert_array_equal(host(rf.weights).view(np.uint32), wf.view(np.uint32))
+    np.testing.assert_array_equal(bf16_bits(rf.weights_bf16), wb)
+    # R3 lists
+    off, pairs = orc.routing_lists(ids, synth.E)
+    np.testing.assert_array_equal(host(rf.offsets), off)
+    np.testing.assert_array_equal(host(rf.pairs), pairs)
+    # R4 MXFP8
+    q, sc = orc.mxfp8_quantize(d["latent"])
+    np.testing.assert_array_equal(host(rf.q), q)
+    np.testing.assert_array_equal(host(rf.scales), sc)
+    # R5 Finalize with the BF16 weights (the wide path's Finalize input)
+    np.testing.assert_array_equal(bf16_bits(rf.out), orc.finalize(d["rows"], wb, T, synth.K))
+
+
+def test_tiny(moe, orc):
+    _check_chain(moe, orc, 8)
+
+
+def test_narrow(moe, orc):
+    _check_chain(moe, orc, 64)
+
+
+def test_wide(moe, orc):
+    _check_chain(moe, orc, 1020, samples=4000)
+
+
+@pytest.mark.parametrize("T", [1, 16, 256, 4096])
+def test_skew_sweep(moe, orc, T):
+    _check_chain(moe, orc, T, skew=True, samples=None if T <= 16 else 3000)
+
+
+def test_wide_in_cuda_graph(moe, orc):
+    _check_chain(moe, orc, 1020, samples=2000, graph=True)

@@ -1,0 +1,57 @@
+"""MXFP8 quantisation on the GPU against the oracle, bit for bit (OCP MX reading of
+the pages' "MXFP8 activations")."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import bf16_dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(moe, orc, x):
+    q, s = moe.mxfp8_quantize_rows(bf16_dev(x))
+    torch.cuda.synchronize()
+    eq, es = orc.mxfp8_quantize(x)
+    np.testing.assert_array_equal(host(s), es)
+    np.testing.assert_array_equal(host(q), eq)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 3584), (8, 3584), (1020, 3584), (4096, 3584), (3, 32), (7, 96), (33, 288), (5, 7168)])
+def test_normal_rows(moe, orc, rows, cols):
+    _compare(moe, orc, synth.normal_bf16(30 + rows, 5, (rows, cols)))
+
+
+def test_wide_dynamic_range(moe, orc):
+    rng = np.random.default_rng(31)
+    f = (rng.normal(0, 1, (64, 1024)) * np.exp2(rng.integers(-140, 128, (64, 1)))).astype(np.float32)
+    f[np.isinf(f)] = 0
+    _compare(moe, orc, synth.f32_to_bf16_bits(f))
+
+
+def test_special_blocks(moe, orc):
+    x = synth.normal_bf16(32, 5, (4, 256))
+    x[0, 0:32] = 0
+    x[0, 32:64] = 0x8000
+    x[1, 0:32] = 0x0001
+    x[1, 40] = 0x7F80          # +inf
+    x[2, 70] = 0x7FC0          # NaN
+    x[2, 100] = 0xFF80         # -inf
+    x[3, 0:32] = 0x7F7F        # max finite
+    x[3, 32:64] = np.arange(32, dtype=np.uint16) | 0x8000  # negative subnormals
+    _compare(moe, orc, x)
+
+
+@pytest.mark.parametrize("amax_bits", [0x3F80, 0x4B00, 0x0080, 0x7F00, 0x2000, 0x0001, 0x43E0])
+def test_exhaustive_patterns(moe, orc, amax_bits):
+    b = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    f = synth.bf16_bits_to_f32(b)
+    amax = synth.bf16_bits_to_f32(np.array([amax_bits], np.uint16))[0]
+    vals = b[np.isfinite(f) & (np.abs(f) <= amax)]
+    n = -(-vals.size // 31)
+    body = np.resize(vals, n * 31).reshape(n, 31)
+    x = np.concatenate([np.full((n, 1), amax_bits, np.uint16), body], axis=1)
+    pad = (-x.shape[0]) % 4
+    x = np.concatenate([x, np.zeros((pad, 32), np.uint16)]).reshape(-1, 128)
+    _compare(moe, orc, x)

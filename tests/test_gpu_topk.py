@@ -1,0 +1,85 @@
+"""Sigmoid + bias top-K on the GPU against the oracle (which consumes the same
+logits): ids, FP32 and BF16 weights bit for bit (DEP page, EpMoeLayer.topk; wide
+page, WideRoute "exact top16 and renormalized weights")."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import bf16_bits, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(moe, orc, logits, bias, K, renorm=True, scale=1.0):
+    ids, w, wb = moe.topk_route(dev(logits), None if bias is None else dev(bias), K, renorm, scale)
+    torch.cuda.synchronize()
+    eids, ew, ewb = orc.topk_route(logits, bias, K, renorm, scale)
+    np.testing.assert_array_equal(host(ids), eids)
+    np.testing.assert_array_equal(host(w).view(np.uint32), ew.view(np.uint32))
+    np.testing.assert_array_equal(bf16_bits(wb), ewb)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 1020, 4096])
+def test_decode_shapes(moe, orc, T):
+    logits = synth.normal_f32(20 + T, 1, (T, 896), 1.7)
+    _compare(moe, orc, logits, synth.correction_bias(), 16)
+
+
+def test_skew_bias(moe, orc):
+    logits = synth.normal_f32(21, 1, (512, 896), 1.7)
+    _compare(moe, orc, logits, synth.skew_bias(), 16)
+
+
+@pytest.mark.parametrize("E,K", [(1, 1), (16, 16), (33, 4), (127, 16), (128, 32), (129, 8), (1000, 16), (1024, 32), (896, 1)])
+def test_expert_counts(moe, orc, E, K):
+    logits = synth.normal_f32(22 + E, 1, (45, E), 2.0)
+    _compare(moe, orc, logits, synth.normal_f32(22 + E, 3, (E,), 0.05), K)
+
+
+@pytest.mark.parametrize("renorm,scale,bias", [(False, 1.0, True), (True, 2.5, True), (False, 0.5, False), (True, 1.0, False)])
+def test_flags(moe, orc, renorm, scale, bias):
+    logits = synth.normal_f32(23, 1, (77, 896), 1.7)
+    _compare(moe, orc, logits, synth.correction_bias() if bias else None, 16, renorm, scale)
+
+
+def test_heavy_ties_fallback(moe, orc):
+    """Saturated sigmoids (exactly 0 or 1) and a coarse bias grid: many equal keys, more
+    than 64 candidates above the bound, so the warp takes the argmax-rounds path."""
+    rng = np.random.default_rng(24)
+    logits = rng.choice(np.array([-100.0, 20.0, 0.0], np.float32), size=(64, 896)).astype(np.float32)
+    bias = (rng.integers(-2, 3, 896) / 16.0).astype(np.float32)
+    _compare(moe, orc, logits, bias, 16)
+    _compare(moe, orc, np.zeros((8, 896), np.float32), None, 16)  # every key equal
+
+
+def test_special_values(moe, orc):
+    rng = np.random.default_rng(25)
+    logits = rng.normal(0, 30, (32, 256)).astype(np.float32)
+    logits[:, ::7] = np.float32(np.inf)
+    logits[:, 3::11] = -np.float32(np.inf)
+    logits[:, 5::13] = 17.5
+    logits[:, 6::17] = -88.5
+    logits[:, 1::19] = 1e-40  # subnormal input
+    _compare(moe, orc, logits, synth.normal_f32(25, 3, (256,), 0.01), 16)
+
+
+@pytest.mark.slow
+def test_sigmoid_exhaustive(moe, orc):
+    """The specified sigmoid, GPU against oracle, for every FP32 bit pattern (E = K = 1,
+    no renormalisation: the weight is the score)."""
+    chunk = 1 << 26
+    threads = os.cpu_count() or 4
+    for start in range(0, 1 << 32, chunk):
+        u = (np.arange(start, start + chunk, dtype=np.uint64)).astype(np.uint32)
+        x = u.view(np.float32).reshape(chunk, 1)
+        _, w, _ = moe.topk_route(dev(x), None, 1, False, 1.0, want_bf16=False)
+        got = host(w).reshape(-1)
+        parts = np.array_split(x.reshape(-1), threads)
+        with ThreadPoolExecutor(threads) as ex:
+            exp = np.concatenate(list(ex.map(orc.sigmoid, parts)))
+        same = (got.view(np.uint32) == exp.view(np.uint32)) | (np.isnan(got) & np.isnan(exp))
+        assert same.all(), f"mismatch at 0x{int(u[~same][0]):08x}"
