@@ -124,6 +124,75 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+class Step:
+    """Device-resident inputs and preallocated buffers of one routing-and-combine step,
+    plus the step captured as a CUDA graph."""
+
+    def __init__(self, T, device, seed=0, skew=False, router_algo=0, graph=True):
+        import torch
+
+        import latent_moe_decode_gb300 as m
+
+        self.m, self.T, self.device = m, T, device
+        self.host = synth.chain_inputs(T, seed=seed, skew=skew)
+        d = self.host
+        tob = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+        self.x, self.w, self.latent, self.rows = tob(d["x"]), tob(d["w"]), tob(d["latent"]), tob(d["rows"])
+        self.bias = torch.from_numpy(d["bias"]).to(device)
+        self.rf = m.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K, device=device, router_algo=router_algo)
+        self.graph = None
+        if graph:
+            s = torch.cuda.Stream(device)
+            s.wait_stream(torch.cuda.current_stream(device))
+            with torch.cuda.stream(s):
+                self.run_direct()
+            torch.cuda.current_stream(device).wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.run_direct()
+            self.graph = g
+
+    def run_direct(self):
+        self.rf.run(self.x, self.w, self.bias, self.latent, self.rows)
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.run_direct()
+
+    def calls(self):
+        m, rf, T = self.m, self.rf, self.T
+        return {
+            "router": lambda: m.router_logits(self.x, self.w, out=rf.logits, workspace=rf.router_ws, algo=rf.router_algo),
+            "topk": lambda: m.topk_route(rf.logits, self.bias, synth.K, ids=rf.ids, weights=rf.weights, weights_bf16=rf.weights_bf16),
+            "lists": lambda: m.build_routing_lists(rf.ids, synth.E, offsets=rf.offsets, pairs=rf.pairs, workspace=rf.lists_ws),
+            "mxfp8": lambda: m.mxfp8_quantize_rows(self.latent, q=rf.q, scales=rf.scales),
+            "finalize": lambda: m.finalize(self.rows, rf.weights_bf16, T, synth.K, out=rf.out),
+        }
+
+
+SLEEP_CYCLES = 200_000  # ~100 us of GPU spin so the host is ahead when the timed work starts
+
+
+def time_region(fn, n, flush, stream):
+    """CUDA-event times of fn() over n repetitions; before each one L2 is flushed and
+    the GPU spins briefly (both outside the events) so the launch is already queued."""
+    import torch
+
+    evs = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        torch.cuda._sleep(SLEEP_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -133,11 +202,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     m.load()
     T = T_WIDE
-    d = synth.chain_inputs(T, seed=rank)
-    tob = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-    x, w, latent, rows = tob(d["x"]), tob(d["w"]), tob(d["latent"]), tob(d["rows"])
-    bias = torch.from_numpy(d["bias"]).to(dev)
-    rf = m.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K, device=dev)
+    step = Step(T, dev, seed=rank)
+    rf = step.rf
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -148,44 +214,21 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         flush.fill_(1)
-        rf.run(x, w, bias, latent, rows)
+        step.run()
     barrier()
 
-    # (a) the chain, L2 flushed before every step (outside the step's events)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
+        # (a) the whole step (CUDA graph of the five calls), cold L2 every step
         barrier()
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            rf.run(x, w, bias, latent, rows)
-            ev[i][1].record(stream)
+        step_ms = time_region(step.run, args.steps, flush, stream)
         barrier()
-        step_ms = [a.elapsed_time(b) for a, b in ev]
-
         # (b) each call alone (cold L2) for the per-kernel roofline
-        calls = {
-            "router": lambda: m.router_logits(x, w, out=rf.logits, workspace=rf.router_ws),
-            "topk": lambda: m.topk_route(rf.logits, bias, synth.K, ids=rf.ids, weights=rf.weights, weights_bf16=rf.weights_bf16),
-            "lists": lambda: m.build_routing_lists(rf.ids, synth.E, offsets=rf.offsets, pairs=rf.pairs, workspace=rf.lists_ws),
-            "mxfp8": lambda: m.mxfp8_quantize_rows(latent, q=rf.q, scales=rf.scales),
-            "finalize": lambda: m.finalize(rows, rf.weights_bf16, T, synth.K, out=rf.out),
-        }
-        per = {k: [] for k in calls}
-        for i in range(args.steps):
-            for k, fn in calls.items():
-                flush.fill_(i & 0xFF)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn()
-                b.record(stream)
-                per[k].append((a, b))
-        barrier()
-        per_ms = {k: float(np.mean([a.elapsed_time(b) for a, b in v])) for k, v in per.items()}
+        per_ms = {k: float(np.mean(time_region(fn, args.steps, flush, stream))) for k, fn in step.calls().items()}
     clocks = clk.summary()
     assert m.device_error(clear=True) == 0
 
     # (c) end to end through the public API: pinned host inputs in, results out
+    d = step.host
     hx = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hl = torch.from_numpy(d["latent"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hr = torch.from_numpy(d["rows"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -195,10 +238,10 @@ def run_ours(args, rank, world, local_rank):
     d2h = sum(t.numel() * t.element_size() for t in houts)
 
     def e2e_step():
-        x.copy_(hx, non_blocking=True)
-        latent.copy_(hl, non_blocking=True)
-        rows.copy_(hr, non_blocking=True)
-        rf.run(x, w, bias, latent, rows)
+        step.x.copy_(hx, non_blocking=True)
+        step.latent.copy_(hl, non_blocking=True)
+        step.rows.copy_(hr, non_blocking=True)
+        step.run_direct()
         for h, o in zip(houts, outs):
             h.copy_(o, non_blocking=True)
 
@@ -226,7 +269,7 @@ def run_ours(args, rank, world, local_rank):
     fin_gbs = ab["finalize"] / (per_ms["finalize"] * 1e-3) / 1e9
     traffic = kernel_traffic("finalize")
     steps = {}
-    for k in calls:
+    for k in per_ms:
         gbs = ab[k] / (per_ms[k] * 1e-3) / 1e9
         steps[k] = {"us": round(per_ms[k] * 1e3, 2), "alg_bytes": ab[k], "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
     flops = 2.0 * T * synth.E * synth.H
@@ -247,11 +290,12 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; shapes and distributions of the pages' wide decode batch)",
         "config": {"workload": WORKLOAD, "T": T, "hidden": synth.H, "latent": synth.L, "experts": synth.E, "top_k": synth.K,
                    "l2": "flushed (256 MB write) before every timed step, outside its events",
+                   "launch": "the step's kernels captured once in a CUDA graph, programmatic dependent launch between them",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "chain_GB/s": round(sum(ab.values()) / (ms * 1e-3) / 1e9, 1),
         "roofline": {"kernel": "finalize", "bound": "hbm", "achieved": round(fin_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(fin_gbs / hbm, 3), "traffic": traffic, "alg_bytes_per_launch": ab["finalize"],
-                     "peak_source": f"{peak_src} (copy bandwidth, MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"},
+                     "peak_source": f"{peak_src}: copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"},
         "steps_alone": steps,
         "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -261,6 +305,56 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+def run_sweep(args):
+    """The skew sweep: the whole step per T with Zipf(1.1) expert popularity, plus each
+    call alone; one JSON line per T."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    hbm = load_peaks()[0]
+    for T in [int(t) for t in args.sweep.split(",")]:
+        for algo in ([0] if not args.router_algos else [int(a) for a in args.router_algos.split(",")]):
+            step = Step(T, dev, skew=True, router_algo=algo)
+            for _ in range(args.warmup):
+                step.run()
+            ms = float(np.mean(time_region(step.run, args.steps, flush, stream)))
+            per = {k: round(float(np.mean(time_region(fn, args.steps, flush, stream))) * 1e3, 2) for k, fn in step.calls().items()}
+            stock = None
+            try:  # the stock router call of the pages (cuBLAS through torch), for context
+                out = torch.empty(T, synth.E, dtype=torch.float32, device=dev)
+                mm = lambda: torch.mm(step.x, step.w.t(), out_dtype=torch.float32, out=out)
+                mm()
+                stock = round(float(np.mean(time_region(mm, args.steps, flush, stream))) * 1e3, 2)
+            except Exception:
+                pass
+            loads = np.bincount(step.rf.ids.cpu().numpy().ravel(), minlength=synth.E)
+            ab = algorithmic_bytes(T)
+            print(json.dumps({"T": T, "router_algo": algo, "us_per_step": round(ms * 1e3, 2),
+                              "tokens/s": round(T / (ms * 1e-3), 1), "chain_GB/s": round(sum(ab.values()) / (ms * 1e-3) / 1e9, 1),
+                              "frac_hbm_chain": round(sum(ab.values()) / (ms * 1e-3) / 1e9 / hbm, 3), "us_alone": per,
+                              "us_stock_router_torch_mm": stock,
+                              "expert_load_max_over_mean": round(float(loads.max() / max(loads.mean(), 1e-9)), 2)}), flush=True)
+            assert m.device_error(clear=True) == 0
+            del step
+            torch.cuda.empty_cache()
+
+
+def run_ncu_step(args):
+    """The wide step, untimed, warmup + steps times (for profiler captures)."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    step = Step(args.T or T_WIDE, dev, graph=False, router_algo=args.router_algo)
+    for _ in range(args.warmup + args.steps):
+        step.run()
+    torch.cuda.synchronize()
 
 
 # ---------------------------------------------------------------------------
@@ -321,12 +415,23 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None, help="comma-separated T list: the skew sweep, one JSON line per T")
+    ap.add_argument("--router-algos", default=None, help="with --sweep: router kernel families to time (0 auto, 1 simt, 2 tcgen05)")
+    ap.add_argument("--ncu-step", action="store_true", help="run the step untimed (for profiler captures)")
+    ap.add_argument("--T", type=int, default=0, help="with --ncu-step: token count (default 1020)")
+    ap.add_argument("--router-algo", type=int, default=0, help="with --ncu-step: router kernel family")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.ncu_step:
+        run_ncu_step(args)
+        return
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank)
     else:

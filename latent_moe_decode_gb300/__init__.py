@@ -232,9 +232,8 @@ class RouteFinalize:
 
     def _count_launches(self) -> int:
         """Kernels one run() launches."""
-        # router (+ split-K reduce), top-k, lists (1 or 2), MXFP8, Finalize
-        return 5 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0) + (
-            1 if build_routing_lists_workspace(self.T, self.K, self.E) > 0 else 0)
+        # router (+ its split-K reduce when it needs scratch), top-k, lists, MXFP8, Finalize
+        return 5 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0)
 
     def run(self, x, w, bias, latent, rows, stream=None):
         router_logits(x, w, out=self.logits, workspace=self.router_ws, algo=self.router_algo, stream=stream)

@@ -1,4 +1,4 @@
-// Per-expert routing lists: a deterministic counting sort of the (token, slot) pairs.
+// Per-expert routing lists: a deterministic, atomics-free counting sort.
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideRoute
 // (docstring and kernel): each of token t's pairs is appended to its expert's list as
@@ -6,196 +6,204 @@
 // relaxed atomic counter, so their list order is arbitrary; here every list is in
 // ascending token order and stored as CSR (offsets = exclusive prefix sum of counts).
 //
-// GB300 design: one CTA of 32 warps per chunk of 1024 tokens; lane l of warp w owns
-// token 32 w + l. For each slot k the warp groups equal expert ids with match.any; the
-// group's lowest lane ORs the group's lane mask into M[w][e] in shared memory (one
-// writer per word per step, so no atomics). Then per expert: P[w][e] = the tokens of
-// warps before w that chose e (prefix of popc(M)), counts = popc sums, offsets = a
-// block scan over experts, and a pair lands at
-//   offsets[e] + (pairs of earlier chunks) + P[w][e] + popc(M[w][e] & lanes below l).
-// Up to 1024 tokens need one launch; beyond, a counting launch writes per-chunk counts
-// to the workspace and a placing launch adds the earlier chunks' counts.
+// GB300 design: the pair code of ids[t, k] is its flat index i = t*K + k, so for an
+// expert e
+//   offsets[e]             = #{ i : 0 <= ids[i] < e }
+//   pairs[offsets[e] + r]  = the r-th i (ascending) with ids[i] == e
+// i.e. an order-preserving filter of the flat id array. That array is small (T*K*4
+// bytes, L2-resident), so every CTA scans all of it and owns a range of up to 8
+// experts: no cross-CTA scan, no workspace, no atomics. Inside a CTA the 16 warps
+// split the ids into contiguous ranges, loaded 1024 at a time (8 int4 per lane in
+// flight; the first batch stays in registers for pass 2). Pass 1 counts, per warp, the
+// ids below the CTA's first expert and the matches of each owned expert (8-bit fields
+// of a 64-bit counter); the CTA then knows where each warp's run of each expert
+// starts. Pass 2 writes every match at start[warp][expert] + the warp's running count
+// + the count in the lanes below (one 64-bit packed warp scan ranks all owned experts).
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kChunk = 1024;  // tokens per CTA (32 warps x 32 lanes)
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxEpc = 8;  // experts per CTA: 8-bit fields of a 64-bit counter
+constexpr int kBatch = 8;   // int4 loads in flight per lane (1024 ids per warp per batch)
 constexpr unsigned kFull = 0xFFFFFFFFu;
-
-enum Mode { kSingle = 0, kCount = 1, kPlace = 2 };
 
 struct ListArgs {
   const int32_t* ids;
-  int T, K, E;
+  long long n;  // T * K
+  int E, epc;
   int32_t* offsets;
   int32_t* pairs;
-  int32_t* counts;  // [nchunks][E] workspace (kCount / kPlace)
-  int nchunks;
   uint32_t* err;
+  int vec;  // ids may be read as int4
 };
 
-size_t smem_bytes(int E) { return (size_t)32 * E * 4 + (size_t)32 * E * 2 + (size_t)(E + 1) * 4 + 32 * 4; }
-
-// Exclusive scan of one value per thread over a 1024-thread block; *total gets the sum.
-__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_sums[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    const int ws = warp_sums[lane];
-    int wi = ws;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi += y;
-    }
-    warp_sums[lane] = wi - ws;  // exclusive warp offsets
-    if (lane == 31) *total = wi;
-  }
-  __syncthreads();
-  const int r = warp_sums[w] + incl - v;
-  __syncthreads();
-  return r;
+// ids i0..i0+3; entries at or past `end` read as -1 (never below e_lo, never a match)
+__device__ __forceinline__ int4 load4(const ListArgs& a, long long i0, long long end) {
+  if (a.vec && i0 + 3 < end) return __ldg(reinterpret_cast<const int4*>(a.ids + i0));
+  int4 v;
+  v.x = i0 < end ? __ldg(a.ids + i0) : -1;
+  v.y = i0 + 1 < end ? __ldg(a.ids + i0 + 1) : -1;
+  v.z = i0 + 2 < end ? __ldg(a.ids + i0 + 2) : -1;
+  v.w = i0 + 3 < end ? __ldg(a.ids + i0 + 3) : -1;
+  return v;
 }
 
-// KMAX: compile-time bound on K (16 or 32), the size of the per-thread id array.
-template <int MODE, int KMAX>
-__global__ void __launch_bounds__(1024) lists_kernel(const ListArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int E = a.E, K = a.K;
-  uint32_t* M = reinterpret_cast<uint32_t*>(smem);           // [32][E] lane masks
-  uint16_t* P = reinterpret_cast<uint16_t*>(M + 32 * E);     // [32][E] warp prefixes
-  int32_t* base = reinterpret_cast<int32_t*>(P + 32 * E);    // [E + 1]
-  int32_t* warp_sums = base + E + 1;                         // [32]
-  __shared__ int total_sh;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int chunk = blockIdx.x;
+__device__ __forceinline__ void unpack_add(int (&c)[kMaxEpc], unsigned long long p) {
+#pragma unroll
+  for (int j = 0; j < kMaxEpc; ++j) c[j] += (int)((p >> (8 * j)) & 0xFFu);
+}
+
+__global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
+  __shared__ int s_below[kWarps];
+  __shared__ int s_cnt[kWarps][kMaxEpc];
+  __shared__ int s_start[kWarps][kMaxEpc];
+  __shared__ int s_base[kMaxEpc + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e_lo = blockIdx.x * a.epc;
+  const int nexp = min(a.epc, a.E - e_lo);
+  // warp w scans flat ids [r0, r1): 128 per step, 4 per lane, lanes in order
+  const long long per = ((a.n + kWarps - 1) / kWarps + 127) / 128 * 128;
+  const long long r0 = min(a.n, (long long)warp * per), r1 = min(a.n, r0 + per);
+  const unsigned long long one = 1ull;
 
   grid_launch_dependents();
   grid_wait();
-  for (int i = tid; i < 32 * E; i += kChunk) M[i] = 0u;
 
-  const int t = chunk * kChunk + tid;
-  const bool live = t < a.T;
-  int my_e[KMAX];
+  // pass 1 (the first batch of ids stays in registers for pass 2)
+  int below = 0;
+  int cnt[kMaxEpc];
 #pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    int e = -1;
-    if (live && k < K) {
-      e = __ldg(a.ids + (size_t)t * K + k);
-      if (e < 0 || e >= E) {
-        set_error(a.err, MOE_DEVERR_EXPERT_ID);
-        e = -1;
+  for (int j = 0; j < kMaxEpc; ++j) cnt[j] = 0;
+  bool bad = false;
+  int4 held[kBatch];
+  for (long long b0 = r0; b0 < r1; b0 += kBatch * 128) {
+    int4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) v[u] = load4(a, b0 + 128 * u + 4 * lane, r1);
+    unsigned long long acc = 0;  // 8-bit fields: at most 4 * kBatch per lane
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        below += (unsigned)q[m] < (unsigned)e_lo;
+        const unsigned jv = (unsigned)(q[m] - e_lo);
+        if (jv < (unsigned)nexp) acc += one << (8 * jv);
+        bad |= (unsigned)q[m] >= (unsigned)a.E && b0 + 128 * u + 4 * lane + m < r1;
       }
+      if (b0 == r0) held[u] = v[u];
     }
-    my_e[k] = e;
+    unpack_add(cnt, acc);
   }
-  __syncthreads();
-  uint32_t* Mw = M + w * E;
+  if (blockIdx.x == 0 && __any_sync(kFull, bad) && lane == 0) set_error(a.err, MOE_DEVERR_EXPERT_ID);
+  below = __reduce_add_sync(kFull, below);
 #pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    if (k < K) {  // uniform across the block
-      const unsigned g = __match_any_sync(kFull, my_e[k]);
-      if (my_e[k] >= 0 && lane == __ffs(g) - 1) Mw[my_e[k]] |= g;
-      __syncwarp();
-    }
+  for (int j = 0; j < kMaxEpc; ++j) cnt[j] = __reduce_add_sync(kFull, cnt[j]);
+  if (lane == 0) {
+    s_below[warp] = below;
+#pragma unroll
+    for (int j = 0; j < kMaxEpc; ++j) s_cnt[warp][j] = cnt[j];
   }
   __syncthreads();
 
-  // per expert: warp prefixes and this chunk's count
-  int cnt = 0;
-  const int e_own = tid;  // E <= 1024: one expert per thread
-  if (e_own < E) {
-    int run = 0;
-    for (int ww = 0; ww < 32; ++ww) {
-      P[ww * E + e_own] = (uint16_t)run;
-      run += __popc(M[ww * E + e_own]);
+  // offsets of the owned experts, and where each warp's run of each expert starts
+  if (threadIdx.x == 0) {
+    int base = 0;
+    for (int w = 0; w < kWarps; ++w) base += s_below[w];
+    for (int j = 0; j < nexp; ++j) {
+      s_base[j] = base;
+      for (int w = 0; w < kWarps; ++w) base += s_cnt[w][j];
     }
-    cnt = run;
+    s_base[nexp] = base;
   }
-  if (MODE == kCount) {
-    if (e_own < E) a.counts[(size_t)chunk * E + e_own] = cnt;
-    return;
-  }
-  int pre = 0, all = cnt;
-  if (MODE == kPlace && e_own < E) {
-    all = 0;
-    for (int c = 0; c < a.nchunks; ++c) {
-      const int v = a.counts[(size_t)c * E + e_own];
-      all += v;
-      if (c < chunk) pre += v;
+  __syncthreads();
+  if (threadIdx.x < kWarps * kMaxEpc) {
+    const int w = threadIdx.x / kMaxEpc, j = threadIdx.x % kMaxEpc;
+    if (j < nexp) {
+      int start = s_base[j];
+      for (int ww = 0; ww < w; ++ww) start += s_cnt[ww][j];
+      s_start[w][j] = start;
     }
   }
-  const int excl = block_exclusive_scan(e_own < E ? all : 0, warp_sums, &total_sh);
-  if (e_own < E) {
-    base[e_own] = excl + pre;
-    if (chunk == 0) a.offsets[e_own] = excl;
-  }
-  if (chunk == 0 && tid == 0) a.offsets[E] = total_sh;
+  if (threadIdx.x < nexp || (threadIdx.x == nexp && e_lo + nexp == a.E)) a.offsets[e_lo + threadIdx.x] = s_base[threadIdx.x];
   __syncthreads();
 
-  if (live) {
-    const unsigned below = (1u << lane) - 1u;
+  // pass 2
+  int run[kMaxEpc];
 #pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      if (k < K && my_e[k] >= 0) {
-        const int e = my_e[k];
-        const int pos = base[e] + P[w * E + e] + __popc(Mw[e] & below);
-        a.pairs[pos] = t * K + k;
+  for (int j = 0; j < kMaxEpc; ++j) run[j] = j < nexp ? s_start[warp][j] : 0;
+  for (long long b0 = r0; b0 < r1; b0 += kBatch * 128) {
+    int4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) v[u] = (b0 == r0) ? held[u] : load4(a, b0 + 128 * u + 4 * lane, r1);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const long long b = b0 + 128 * u;
+      if (b >= r1) break;  // warp-uniform
+      const int q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      unsigned long long mine = 0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const unsigned jv = (unsigned)(q[m] - e_lo);
+        if (jv < (unsigned)nexp) mine += one << (8 * jv);
       }
+      unsigned long long incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned long long total = __shfl_sync(kFull, incl, 31);
+      if (mine) {
+        unsigned long long excl = incl - mine;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const unsigned jv = (unsigned)(q[m] - e_lo);
+          if (jv < (unsigned)nexp) {
+            int r = 0;
+#pragma unroll
+            for (int j = 0; j < kMaxEpc; ++j)
+              if (j == (int)jv) r = run[j];
+            a.pairs[r + (int)((excl >> (8 * jv)) & 0xFFu)] = (int32_t)(b + 4 * lane + m);
+            excl += one << (8 * jv);  // a later id of the same expert among these 4
+          }
+        }
+      }
+      unpack_add(run, total);
     }
   }
-}
-
-template <int KMAX>
-int launch_all(const ListArgs& a, size_t smem, cudaStream_t s) {
-  if (a.nchunks == 1) {
-    if (cudaFuncSetAttribute(lists_kernel<kSingle, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    return launch_pdl(lists_kernel<kSingle, KMAX>, dim3(1), dim3(kChunk), smem, s, a);
-  }
-  if (cudaFuncSetAttribute(lists_kernel<kCount, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(lists_kernel<kPlace, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  const int st = launch_pdl(lists_kernel<kCount, KMAX>, dim3(a.nchunks), dim3(kChunk), smem, s, a);
-  if (st != MOE_OK) return st;
-  return launch_pdl(lists_kernel<kPlace, KMAX>, dim3(a.nchunks), dim3(kChunk), smem, s, a);
 }
 
 }  // namespace
 }  // namespace moe
 
 extern "C" size_t moe_build_routing_lists_workspace(int T, int K, int E) {
-  if (T <= moe::kChunk || E < 1) return 0;
+  (void)T;
   (void)K;
-  const size_t nchunks = ((size_t)T + moe::kChunk - 1) / moe::kChunk;
-  return nchunks * (size_t)E * sizeof(int32_t);
+  (void)E;
+  return 0;
 }
 
 extern "C" int moe_build_routing_lists(const int32_t* ids, int T, int K, int E, int32_t* offsets,
                                        int32_t* pairs, void* workspace, size_t workspace_bytes,
                                        moe_stream_t stream) {
   using namespace moe;
+  (void)workspace;
+  (void)workspace_bytes;
   if (T < 0 || K < 1 || E < 1) return MOE_ERR_INVALID_ARGUMENT;
   if (K > MOE_MAX_TOPK || E > MOE_MAX_EXPERTS) return MOE_ERR_CAPACITY;
   if ((long long)T * K > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
   if (!offsets || (T > 0 && (!ids || !pairs))) return MOE_ERR_INVALID_ARGUMENT;
   if (!aligned(offsets, 4) || (ids && !aligned(ids, 4)) || (pairs && !aligned(pairs, 4))) return MOE_ERR_ALIGNMENT;
-  const size_t need = moe_build_routing_lists_workspace(T, K, E);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 4))) return MOE_ERR_WORKSPACE;
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
-  const int nchunks = T <= kChunk ? 1 : (T + kChunk - 1) / kChunk;
-  ListArgs a{ids, T, K, E, offsets, pairs, static_cast<int32_t*>(workspace), nchunks, dev.error_word};
-  const size_t smem = smem_bytes(E);
-  cudaStream_t s = as_cuda(stream);
-  return K <= 16 ? launch_all<16>(a, smem, s) : launch_all<MOE_MAX_TOPK>(a, smem, s);
+  int epc = (E + dev.sm_count - 1) / dev.sm_count;
+  epc = epc < 1 ? 1 : (epc > kMaxEpc ? kMaxEpc : epc);
+  const long long n = (long long)T * K;
+  ListArgs a{ids, n, E, epc, offsets, pairs, dev.error_word, (K % 4 == 0 && aligned(ids, 16)) ? 1 : 0};
+  return launch_pdl(lists_kernel, dim3((E + epc - 1) / epc), dim3(kThreads), 0, as_cuda(stream), a);
 }

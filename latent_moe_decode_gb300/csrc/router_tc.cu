@@ -34,7 +34,6 @@ namespace {
 constexpr int kBM = 128;              // experts per CTA (TMEM lanes)
 constexpr int kBK = 64;               // K elements per stage (128 bytes: one swizzle span)
 constexpr int kThreads = 128;         // 4 warps
-constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s per wait
 
 template <int BN>
 struct Cfg {
@@ -45,47 +44,6 @@ struct Cfg {
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_timer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of `bar` with parity `parity`; false (and the timeout bit) after 1 s.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer() - t0 > kTimeoutNs) {
-      set_error(err, MOE_DEVERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -154,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty(i), 1);
     }
     mbar_init(accum, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
   }

@@ -8,21 +8,21 @@
 // Selection key c_e = sigmoid(logit_e) + bias_e; order (c descending, expert index
 // ascending); weights are the unbiased scores over their slot-order FP32 sum.
 //
-// GB300 design: one warp per token. Lane l holds the experts 128 j + 4 l + m (j < NJ,
-// m < 4), loaded as float4, so every load instruction of the warp reads 512
-// contiguous bytes. Selection does not run K serial argmax rounds: the K-th largest
-// of the 32 lane maxima (found with a 15-step bitonic network over shuffles) is a
-// lower bound of the K-th largest key, because K different lanes hold a key at least
-// that large. The few candidates at or above that bound are compacted into shared
-// memory and ranked by counting (key greater, or equal with a lower index); the
+// GB300 design: one CTA of 4 warps per token. Thread i holds the experts i + 128 j
+// (j < NJ), so each load instruction of a warp reads 128 contiguous bytes of the
+// logits row. Selection does not run K serial argmax rounds: the K-th largest of the
+// 128 thread maxima is a lower bound of the K-th largest key (K different threads
+// hold a key at least that large). Each warp sorts its 32 maxima with a bitonic
+// network over shuffles; the bound is the K-th of the four sorted top-K lists. The
+// few candidates at or above it (about 17 of 896 for random scores) are compacted into
+// shared memory and ranked by counting (key greater, or equal with a lower index); the
 // candidate of rank k takes slot k. When more than 64 candidates pass the bound
-// (heavy ties) the warp falls back to K rounds of warp argmax (redux.sync).
+// (heavy ties) the CTA falls back to K rounds of argmax (redux.sync per warp).
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
 constexpr int kListCap = 64;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -91,83 +91,84 @@ struct TopkArgs {
   int32_t* ids;
   float* weights;
   uint16_t* weights_bf16;
-  int vec;  // logits rows and bias may be read as float4
 };
 
-struct WarpSmem {
-  uint32_t key[kListCap];
-  int32_t e[kListCap];
-  float s[kListCap];
-  int32_t slot_id[MOE_MAX_TOPK];
-  float slot_s[MOE_MAX_TOPK];
-};
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
 
 template <int NJ>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) topk_kernel(const TopkArgs a) {
-  __shared__ WarpSmem smem_all[kWarpsPerBlock];
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const int t = blockIdx.x * kWarpsPerBlock + wib;
-  WarpSmem& sm = smem_all[wib];
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+  __shared__ uint32_t s_top[kWarps][32];
+  __shared__ uint32_t s_bound;
+  __shared__ int s_cnt[kWarps];
+  __shared__ uint32_t l_key[kListCap];
+  __shared__ int32_t l_e[kListCap];
+  __shared__ float l_s[kListCap];
+  __shared__ int32_t slot_id[MOE_MAX_TOPK];
+  __shared__ float slot_s[MOE_MAX_TOPK];
+  __shared__ uint32_t r_key[kWarps];
+  __shared__ int32_t r_e[kWarps];
+  __shared__ float r_s[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x;
+  const int E = a.E, K = a.K;
   grid_launch_dependents();
   grid_wait();
-  if (t >= a.T) return;
-  const int E = a.E, K = a.K;
   const float* lg = a.logits + (size_t)t * E;
 
-  // 1) scores and keys of this lane's candidates
-  uint32_t key[NJ * 4];
-  float s[NJ * 4];
+  // 1) scores and keys of this thread's experts tid + 128 j
+  uint32_t key[NJ];
+  float s[NJ];
+  float x[NJ], b[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
-    const int e0 = 128 * j + 4 * lane;
-    float x[4], b[4] = {0.f, 0.f, 0.f, 0.f};
-    if (a.vec && e0 < E) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(lg + e0));
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-      if (a.bias) {
-        const float4 bb = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
-        b[0] = bb.x; b[1] = bb.y; b[2] = bb.z; b[3] = bb.w;
-      }
-    } else {
+    const int e = tid + 128 * j;
+    x[j] = e < E ? __ldg(lg + e) : 0.f;
+    b[j] = (a.bias && e < E) ? __ldg(a.bias + e) : 0.f;
+  }
+  uint32_t tmax = 0;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        x[m] = (e0 + m < E) ? __ldg(lg + e0 + m) : 0.f;
-        if (a.bias && e0 + m < E) b[m] = __ldg(a.bias + e0 + m);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int i = 4 * j + m;
-      const float sv = spec_sigmoid(x[m]);
-      const float c = a.bias ? __fadd_rn(sv, b[m]) : sv;
-      s[i] = sv;
-      key[i] = (e0 + m < E) ? order_key(c) : 0u;
-    }
+  for (int j = 0; j < NJ; ++j) {
+    const int e = tid + 128 * j;
+    const float sv = spec_sigmoid(x[j]);
+    const float c = a.bias ? __fadd_rn(sv, b[j]) : sv;
+    s[j] = sv;
+    key[j] = e < E ? order_key(c) : 0u;
+    tmax = max(tmax, key[j]);
   }
 
-  // 2) bound: the K-th largest lane maximum
-  uint32_t lmax = 0;
-#pragma unroll
-  for (int i = 0; i < NJ * 4; ++i) lmax = max(lmax, key[i]);
-  uint32_t v = lmax;
+  // 2) bound: the K-th largest of the 128 thread maxima
+  uint32_t v = tmax;
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
       const uint32_t o = __shfl_xor_sync(kFull, v, j);
-      const bool ascending = (lane & k) == 0;
-      const bool keep_min = ((lane & j) == 0) == ascending;
-      v = keep_min ? min(v, o) : max(v, o);
+      const bool descending = (lane & k) == 0;
+      const bool keep_max = ((lane & j) == 0) == descending;
+      v = keep_max ? max(v, o) : min(v, o);
     }
   }
-  const uint32_t bound = __shfl_sync(kFull, v, 32 - K);  // ascending: K-th largest
+  s_top[warp][lane] = v;  // descending: lane l holds the warp's (l+1)-th largest
+  __syncthreads();
+  if (lane < K) {  // the K largest maxima of each warp: 4K values, one per thread
+    int rank = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      for (int r = 0; r < K; ++r) {
+        const uint32_t o = s_top[w][r];
+        rank += (o > v) || (o == v && (w < warp || (w == warp && r < lane)));
+      }
+    if (rank == K - 1) s_bound = v;
+  }
+  __syncthreads();
+  const uint32_t bound = s_bound;
 
-  // 3) candidates at or above the bound
+  // 3) candidates at or above the bound, compacted in thread order
   uint32_t flags = 0;
 #pragma unroll
-  for (int i = 0; i < NJ * 4; ++i)
-    if (key[i] != 0u && key[i] >= bound) flags |= 1u << i;
+  for (int j = 0; j < NJ; ++j)
+    if (key[j] != 0u && key[j] >= bound) flags |= 1u << j;
   const int mine = __popc(flags);
   int incl = mine;
 #pragma unroll
@@ -175,70 +176,95 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) topk_kernel(const TopkArg
     const int y = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += y;
   }
-  const int total = __shfl_sync(kFull, incl, 31);
+  if (lane == 31) s_cnt[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    before += w < warp ? s_cnt[w] : 0;
+    total += s_cnt[w];
+  }
 
   if (total <= kListCap) {
-    int pos = incl - mine;
+    int pos = before + incl - mine;
 #pragma unroll
-    for (int i = 0; i < NJ * 4; ++i) {
-      if (flags & (1u << i)) {
-        sm.key[pos] = key[i];
-        sm.e[pos] = 128 * (i >> 2) + 4 * lane + (i & 3);
-        sm.s[pos] = s[i];
+    for (int j = 0; j < NJ; ++j) {
+      if (flags & (1u << j)) {
+        l_key[pos] = key[j];
+        l_e[pos] = tid + 128 * j;
+        l_s[pos] = s[j];
         ++pos;
       }
     }
-    __syncwarp();
-    for (int item = lane; item < total; item += 32) {
-      const uint32_t ki = sm.key[item];
-      const int ei = sm.e[item];
+    __syncthreads();
+    if (tid < total) {
+      const uint32_t ki = l_key[tid];
+      const int ei = l_e[tid];
       int rank = 0;
       for (int q = 0; q < total; ++q) {
-        const uint32_t kq = sm.key[q];
-        rank += (kq > ki) || (kq == ki && sm.e[q] < ei);
+        const uint32_t kq = l_key[q];
+        rank += (kq > ki) || (kq == ki && l_e[q] < ei);
       }
       if (rank < K) {
-        sm.slot_id[rank] = ei;
-        sm.slot_s[rank] = sm.s[item];
+        slot_id[rank] = ei;
+        slot_s[rank] = l_s[tid];
       }
     }
   } else {
-    // heavy ties: K rounds of warp argmax over (key desc, expert asc)
+    // heavy ties: K rounds of argmax over (key desc, expert asc)
     for (int k = 0; k < K; ++k) {
       uint32_t bk = 0;
       int be = 0x7FFFFFFF;
       float bs = 0.f;
 #pragma unroll
-      for (int i = 0; i < NJ * 4; ++i) {
-        if (key[i] > bk) {  // ascending expert order within the lane: first max wins
-          bk = key[i];
-          be = 128 * (i >> 2) + 4 * lane + (i & 3);
-          bs = s[i];
+      for (int j = 0; j < NJ; ++j) {
+        if (key[j] > bk) {  // ascending expert order within the thread: first max wins
+          bk = key[j];
+          be = tid + 128 * j;
+          bs = s[j];
         }
       }
       const uint32_t wk = __reduce_max_sync(kFull, bk);
       const int we = (int)__reduce_min_sync(kFull, bk == wk ? (uint32_t)be : 0x7FFFFFFFu);
-      const float ws = __shfl_sync(kFull, bs, (we & 127) >> 2);
+      const float ws = __shfl_sync(kFull, bs, we & 31);  // expert e lives in thread e % 128
       if (lane == 0) {
-        sm.slot_id[k] = we;
-        sm.slot_s[k] = ws;
+        r_key[warp] = wk;
+        r_e[warp] = we;
+        r_s[warp] = ws;
+      }
+      __syncthreads();
+      uint32_t gk = 0;
+      int ge = 0x7FFFFFFF;
+      float gs = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        if (r_key[w] > gk || (r_key[w] == gk && r_e[w] < ge)) {
+          gk = r_key[w];
+          ge = r_e[w];
+          gs = r_s[w];
+        }
+      }
+      if (tid == 0) {
+        slot_id[k] = ge;
+        slot_s[k] = gs;
       }
 #pragma unroll
-      for (int i = 0; i < NJ * 4; ++i)
-        if (128 * (i >> 2) + 4 * lane + (i & 3) == we) key[i] = 0u;
+      for (int j = 0; j < NJ; ++j)
+        if (tid + 128 * j == ge) key[j] = 0u;
+      __syncthreads();
     }
   }
-  __syncwarp();
+  __syncthreads();
 
   // 4) weights: unbiased scores over their slot-order FP32 sum
-  float S = 0.f;
-  for (int k = 0; k < K; ++k) S = __fadd_rn(S, sm.slot_s[k]);
-  if (lane < K) {
-    const float sv = sm.slot_s[lane];
+  if (tid < K) {
+    float S = 0.f;
+    for (int k = 0; k < K; ++k) S = __fadd_rn(S, slot_s[k]);
+    const float sv = slot_s[tid];
     float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(sv, S)) : sv;
     if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
-    const size_t o = (size_t)t * K + lane;
-    a.ids[o] = sm.slot_id[lane];
+    const size_t o = (size_t)t * K + tid;
+    a.ids[o] = slot_id[tid];
     if (a.weights) a.weights[o] = w;
     if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
   }
@@ -261,9 +287,8 @@ extern "C" int moe_topk_route(const float* logits, const float* bias, int T, int
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
-  const int vec = (E % 4 == 0) && aligned(logits, 16) && (!bias || aligned(bias, 16));
-  TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16, vec};
-  dim3 grid((T + kWarpsPerBlock - 1) / kWarpsPerBlock), block(kWarpsPerBlock * 32);
+  TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
+  dim3 grid(T), block(kThreads);
   cudaStream_t s = as_cuda(stream);
   switch ((E + 127) / 128) {
     case 1: return launch_pdl(topk_kernel<1>, grid, block, 0, s, a);

@@ -82,9 +82,9 @@ def test_validation_before_any_cuda_call(lib):
 
 
 def test_lists_workspace_query(lib):
-    assert lib.moe_build_routing_lists_workspace(1024, 16, 896) == 0
-    assert lib.moe_build_routing_lists_workspace(1025, 16, 896) == 2 * 896 * 4
-    assert lib.moe_build_routing_lists_workspace(4096, 16, 896) == 4 * 896 * 4
+    # the expert-parallel filter needs no scratch at any size
+    for T in (0, 1, 1024, 1025, 4096, 65536):
+        assert lib.moe_build_routing_lists_workspace(T, 16, 896) == 0
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path):
