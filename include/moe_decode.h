@@ -109,6 +109,27 @@ int moe_router_logits(const uint16_t* x, const uint16_t* w, float* logits, int T
 int moe_router_logits_ex(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E,
                          void* workspace, size_t workspace_bytes, int algo, moe_stream_t stream);
 
+/* The router logits for callers that cannot allocate device memory when they call it
+ * -- an engine whose pool owns all device memory after start-up, or a plug-in that is
+ * handed only its inputs and outputs -- and so cannot pass a workspace. The pages have
+ * no counterpart of this call. It computes exactly what moe_router_logits computes
+ * (same kernels, same split-K plan, bit-identical results), but keeps the split-K
+ * partials in a fixed array of MOE_ROUTER_NOALLOC_SCRATCH_BYTES that the library
+ * reserves in the device memory of every GPU that loads it, until the process exits.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - The first call on a device looks up the array's device address with that device
+ *     current (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - Sizes whose partials would not fit (moe_router_logits_workspace(T, H, E) above
+ *     the limit) return MOE_ERR_CAPACITY and launch nothing. With E = 896 every T fits.
+ *   - Every call on a device shares the array and leaves its contents behind; nothing
+ *     in it needs to start at zero. Calls whose kernels overlap on the GPU (other
+ *     streams, other threads) race on it: order them on one stream.
+ * Arguments, requirements and numerics as moe_router_logits. */
+#define MOE_ROUTER_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u)
+int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E,
+                              moe_stream_t stream);
+
 /* -------------------------------------------------------------------------------
  * Sigmoid + e_score_correction_bias top-K with renormalised weights.
  * Source: [ep] EpMoeLayer.topk (one group, sigmoid scoring, correction bias,

@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_router_logits_workspace": (_SZ, [_I, _I, _I]),
     "moe_router_logits": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "moe_router_logits_ex": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _I, _P]),
+    "moe_router_logits_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "moe_build_routing_lists_workspace": (_SZ, [_I, _I, _I]),
     "moe_build_routing_lists": (_I, [_P, _I, _I, _I, _P, _P, _P, _SZ, _P]),

@@ -1,0 +1,56 @@
+"""The allocation-free router entry point, moe_router_logits_noalloc, called through
+the C ABI, against the regular moe_router_logits on the same inputs.
+
+It exists for callers that cannot allocate device memory when they compute the
+router logits (an engine whose memory pool owns the device after start-up, a plug-in
+given only its inputs and outputs): it keeps the split-K partials in an array the
+library reserves itself. Three calls in a row with different shapes check that what
+the previous call left in that shared array never leaks into a result. Kept in a file
+of its own, collected last."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import bf16_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(moe, x, w):
+    T, H = x.shape
+    E = w.shape[0]
+    out = torch.empty(T, E, dtype=torch.float32, device=x.device)
+    st = moe.load().moe_router_logits_noalloc(
+        ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(out.data_ptr()), T, H, E,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, moe.load().moe_status_string(st)
+    return out
+
+
+def test_noalloc_matches_router_logits(moe):
+    torch.backends.cuda.matmul.allow_tf32 = False
+    w = bf16_dev(synth.router_weight())
+    for T, seed in ((1020, 1), (256, 2), (1020, 3)):
+        x = bf16_dev(synth.hidden_rows(T, seed=seed))
+        got = _noalloc(moe, x, w)
+        ref = moe.router_logits(x, w)  # the regular entry point, caller-owned workspace
+        torch.cuda.synchronize()
+        bound = 1e-5 * (x.float().abs() @ w.float().abs().t())
+        assert torch.all((got - ref).abs() <= bound), f"T={T}"
+        assert torch.equal(got, ref), f"T={T}: not bit-identical"
+    assert moe.device_error(clear=True) == 0
+
+
+def test_noalloc_rejects_bad_arguments(moe):
+    lib = moe.load()
+    x = bf16_dev(np.zeros((8, 64), np.uint16))
+    w = bf16_dev(np.zeros((16, 64), np.uint16))
+    out = torch.empty(8, 16, dtype=torch.float32, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.moe_router_logits_noalloc(p(x), p(w), p(out), 0, 64, 16, s) == moe.ERR_INVALID_ARGUMENT
+    assert lib.moe_router_logits_noalloc(p(x), p(w), p(out), 8, 63, 16, s) == moe.ERR_INVALID_ARGUMENT
+    assert lib.moe_router_logits_noalloc(ctypes.c_void_p(x.data_ptr() + 2), p(w), p(out), 8, 64, 16, s) == moe.ERR_ALIGNMENT
