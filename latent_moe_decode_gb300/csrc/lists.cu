@@ -11,14 +11,14 @@
 //   offsets[e]             = #{ i : 0 <= ids[i] < e }
 //   pairs[offsets[e] + r]  = the r-th i (ascending) with ids[i] == e
 // i.e. an order-preserving filter of the flat id array. That array is small (T*K*4
-// bytes, L2-resident), so every CTA scans all of it and owns a range of up to 8
-// experts: no cross-CTA scan, no workspace, no atomics. Inside a CTA the 16 warps
-// split the ids into contiguous ranges, loaded 1024 at a time (8 int4 per lane in
-// flight; the first batch stays in registers for pass 2). Pass 1 counts, per warp, the
-// ids below the CTA's first expert and the matches of each owned expert (8-bit fields
-// of a 64-bit counter); the CTA then knows where each warp's run of each expert
-// starts. Pass 2 writes every match at start[warp][expert] + the warp's running count
-// + the count in the lanes below (one 64-bit packed warp scan ranks all owned experts).
+// bytes, L2-resident), so every CTA scans all of it and owns a range of experts: no
+// cross-CTA scan, no workspace, no global atomics. Inside a CTA the 16 warps split the
+// ids into contiguous ranges, loaded 1024 at a time (8 int4 per lane in flight; the
+// first batch stays in registers for pass 2). Pass 1 counts, per warp, the ids below
+// the CTA's first expert and (shared-memory atomics: counts do not depend on order)
+// the matches of each owned expert; the CTA then knows where each warp's run of each
+// expert starts. Pass 2 ballots which lanes hold a match -- most steps have none -- and
+// writes those few in lane order, so every list stays in ascending index order.
 #include "common.cuh"
 
 namespace moe {
@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxEpc = 8;  // experts per CTA: 8-bit fields of a 64-bit counter
+constexpr int kMaxEpc = 32;  // experts per CTA
 constexpr int kBatch = 8;   // int4 loads in flight per lane (1024 ids per warp per batch)
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -51,15 +51,10 @@ __device__ __forceinline__ int4 load4(const ListArgs& a, long long i0, long long
   return v;
 }
 
-__device__ __forceinline__ void unpack_add(int (&c)[kMaxEpc], unsigned long long p) {
-#pragma unroll
-  for (int j = 0; j < kMaxEpc; ++j) c[j] += (int)((p >> (8 * j)) & 0xFFu);
-}
-
 __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
   __shared__ int s_below[kWarps];
   __shared__ int s_cnt[kWarps][kMaxEpc];
-  __shared__ int s_start[kWarps][kMaxEpc];
+  __shared__ int s_run[kWarps][kMaxEpc];
   __shared__ int s_base[kMaxEpc + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e_lo = blockIdx.x * a.epc;
@@ -67,23 +62,21 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
   // warp w scans flat ids [r0, r1): 128 per step, 4 per lane, lanes in order
   const long long per = ((a.n + kWarps - 1) / kWarps + 127) / 128 * 128;
   const long long r0 = min(a.n, (long long)warp * per), r1 = min(a.n, r0 + per);
-  const unsigned long long one = 1ull;
+  static_assert(kWarps * kMaxEpc == kThreads, "one counter per thread");
+  s_cnt[threadIdx.x / kMaxEpc][threadIdx.x % kMaxEpc] = 0;
+  __syncthreads();
 
   grid_launch_dependents();
   grid_wait();
 
   // pass 1 (the first batch of ids stays in registers for pass 2)
   int below = 0;
-  int cnt[kMaxEpc];
-#pragma unroll
-  for (int j = 0; j < kMaxEpc; ++j) cnt[j] = 0;
   bool bad = false;
   int4 held[kBatch];
   for (long long b0 = r0; b0 < r1; b0 += kBatch * 128) {
     int4 v[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) v[u] = load4(a, b0 + 128 * u + 4 * lane, r1);
-    unsigned long long acc = 0;  // 8-bit fields: at most 4 * kBatch per lane
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
@@ -91,22 +84,15 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
       for (int m = 0; m < 4; ++m) {
         below += (unsigned)q[m] < (unsigned)e_lo;
         const unsigned jv = (unsigned)(q[m] - e_lo);
-        if (jv < (unsigned)nexp) acc += one << (8 * jv);
+        if (jv < (unsigned)nexp) atomicAdd(&s_cnt[warp][jv], 1);
         bad |= (unsigned)q[m] >= (unsigned)a.E && b0 + 128 * u + 4 * lane + m < r1;
       }
       if (b0 == r0) held[u] = v[u];
     }
-    unpack_add(cnt, acc);
   }
   if (blockIdx.x == 0 && __any_sync(kFull, bad) && lane == 0) set_error(a.err, MOE_DEVERR_EXPERT_ID);
   below = __reduce_add_sync(kFull, below);
-#pragma unroll
-  for (int j = 0; j < kMaxEpc; ++j) cnt[j] = __reduce_add_sync(kFull, cnt[j]);
-  if (lane == 0) {
-    s_below[warp] = below;
-#pragma unroll
-    for (int j = 0; j < kMaxEpc; ++j) s_cnt[warp][j] = cnt[j];
-  }
+  if (lane == 0) s_below[warp] = below;
   __syncthreads();
 
   // offsets of the owned experts, and where each warp's run of each expert starts
@@ -120,21 +106,19 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
     s_base[nexp] = base;
   }
   __syncthreads();
-  if (threadIdx.x < kWarps * kMaxEpc) {
+  {
     const int w = threadIdx.x / kMaxEpc, j = threadIdx.x % kMaxEpc;
     if (j < nexp) {
       int start = s_base[j];
       for (int ww = 0; ww < w; ++ww) start += s_cnt[ww][j];
-      s_start[w][j] = start;
+      s_run[w][j] = start;
     }
   }
   if (threadIdx.x < nexp || (threadIdx.x == nexp && e_lo + nexp == a.E)) a.offsets[e_lo + threadIdx.x] = s_base[threadIdx.x];
   __syncthreads();
 
-  // pass 2
-  int run[kMaxEpc];
-#pragma unroll
-  for (int j = 0; j < kMaxEpc; ++j) run[j] = j < nexp ? s_start[warp][j] : 0;
+  // pass 2: the few matches, in lane order
+  int* run = s_run[warp];
   for (long long b0 = r0; b0 < r1; b0 += kBatch * 128) {
     int4 v[kBatch];
 #pragma unroll
@@ -144,35 +128,24 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
       const long long b = b0 + 128 * u;
       if (b >= r1) break;  // warp-uniform
       const int q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      unsigned long long mine = 0;
+      unsigned m4 = 0;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const unsigned jv = (unsigned)(q[m] - e_lo);
-        if (jv < (unsigned)nexp) mine += one << (8 * jv);
-      }
-      unsigned long long incl = mine;
+      for (int m = 0; m < 4; ++m) m4 |= ((unsigned)(q[m] - e_lo) < (unsigned)nexp) ? (1u << m) : 0u;
+      unsigned any = __ballot_sync(kFull, m4 != 0);
+      while (any) {
+        const int l = __ffs(any) - 1;
+        any &= any - 1;
+        if (lane == l) {
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned long long total = __shfl_sync(kFull, incl, 31);
-      if (mine) {
-        unsigned long long excl = incl - mine;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const unsigned jv = (unsigned)(q[m] - e_lo);
-          if (jv < (unsigned)nexp) {
-            int r = 0;
-#pragma unroll
-            for (int j = 0; j < kMaxEpc; ++j)
-              if (j == (int)jv) r = run[j];
-            a.pairs[r + (int)((excl >> (8 * jv)) & 0xFFu)] = (int32_t)(b + 4 * lane + m);
-            excl += one << (8 * jv);  // a later id of the same expert among these 4
+          for (int m = 0; m < 4; ++m) {
+            if (m4 & (1u << m)) {
+              const int jv = q[m] - e_lo;
+              a.pairs[run[jv]++] = (int32_t)(b + 4 * lane + m);
+            }
           }
         }
+        __syncwarp();
       }
-      unpack_add(run, total);
     }
   }
 }

@@ -13,11 +13,12 @@
 // logits row. Selection does not run K serial argmax rounds: the K-th largest of the
 // 128 thread maxima is a lower bound of the K-th largest key (K different threads
 // hold a key at least that large). Each warp sorts its 32 maxima with a bitonic
-// network over shuffles; the bound is the K-th of the four sorted top-K lists. The
-// few candidates at or above it (about 17 of 896 for random scores) are compacted into
-// shared memory and ranked by counting (key greater, or equal with a lower index); the
-// candidate of rank k takes slot k. When more than 64 candidates pass the bound
-// (heavy ties) the CTA falls back to K rounds of argmax (redux.sync per warp).
+// network over shuffles; two rounds of bitonic merging of the four sorted lists give
+// the top 32 of all 128 maxima, whose K-th entry is the bound. The few candidates at
+// or above it (about 17 of 896 for random scores) are compacted into shared memory;
+// up to 32 of them are ordered by one warp-wide bitonic sort of (key, ~expert), so
+// lane k holds slot k (32 < count <= 64: ranked by counting; more, from heavy ties:
+// K rounds of argmax).
 #include "common.cuh"
 
 namespace moe {
@@ -65,13 +66,12 @@ __device__ __forceinline__ float spec_exp(float y) {  // -17.5 < y < 88.5
 }
 
 // sigma(x) = 1 / (1 + exp(-x)), correctly rounded reciprocal; 1 for x >= 17.5,
-// 0 for x <= -88.5, NaN for NaN.
+// 0 for x <= -88.5, NaN for NaN (special cases selected, not branched).
 __device__ __forceinline__ float spec_sigmoid(float x) {
-  if (x != x) return x;
-  if (x >= 17.5f) return 1.0f;
-  if (x <= -88.5f) return 0.0f;
-  const float e = spec_exp(-x);
-  return __frcp_rn(__fadd_rn(1.0f, e));
+  const bool hi = x >= 17.5f, lo = x <= -88.5f;
+  const float e = spec_exp((hi || lo) ? 0.0f : -x);
+  const float r = __frcp_rn(__fadd_rn(1.0f, e));
+  return hi ? 1.0f : (lo ? 0.0f : r);
 }
 
 // Monotone 32-bit key of an FP32 value: larger value -> larger key, -0 == +0,
@@ -99,7 +99,6 @@ constexpr int kWarps = kThreads / 32;
 template <int NJ>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   __shared__ uint32_t s_top[kWarps][32];
-  __shared__ uint32_t s_bound;
   __shared__ int s_cnt[kWarps];
   __shared__ uint32_t l_key[kListCap];
   __shared__ int32_t l_e[kListCap];
@@ -151,18 +150,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   }
   s_top[warp][lane] = v;  // descending: lane l holds the warp's (l+1)-th largest
   __syncthreads();
-  if (lane < K) {  // the K largest maxima of each warp: 4K values, one per thread
-    int rank = 0;
+  // top 32 of the union of two descending lists: max(a[l], b[31-l]) is bitonic;
+  // five half-cleaner steps sort it descending
+  auto merge = [&](uint32_t x, uint32_t y) {
+    uint32_t m = max(x, y);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-      for (int r = 0; r < K; ++r) {
-        const uint32_t o = s_top[w][r];
-        rank += (o > v) || (o == v && (w < warp || (w == warp && r < lane)));
-      }
-    if (rank == K - 1) s_bound = v;
-  }
-  __syncthreads();
-  const uint32_t bound = s_bound;
+    for (int j = 16; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kFull, m, j);
+      m = (lane & j) == 0 ? max(m, o) : min(m, o);
+    }
+    return m;
+  };
+  const uint32_t m01 = merge(s_top[0][lane], s_top[1][31 - lane]);
+  const uint32_t m23 = merge(s_top[2][lane], s_top[3][31 - lane]);
+  const uint32_t top = merge(m01, __shfl_sync(kFull, m23, 31 - lane));
+  const uint32_t bound = __shfl_sync(kFull, top, K - 1);
 
   // 3) candidates at or above the bound, compacted in thread order
   uint32_t flags = 0;
@@ -185,6 +187,51 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     total += s_cnt[w];
   }
 
+  if (total <= 32) {
+    // compact, then one warp sorts (key desc, expert asc): lane k holds slot k
+    int pos = before + incl - mine;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (flags & (1u << j)) {
+        l_key[pos] = key[j];
+        l_e[pos] = tid + 128 * j;
+        l_s[pos] = s[j];
+        ++pos;
+      }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    unsigned long long c = 0;  // (key << 32) | ~expert; 0 = empty
+    float cs = 0.f;
+    if (lane < total) {
+      c = ((unsigned long long)l_key[lane] << 32) | (0xFFFFFFFFu - (uint32_t)l_e[lane]);
+      cs = l_s[lane];
+    }
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const unsigned long long oc = __shfl_xor_sync(kFull, c, j);
+        const float os = __shfl_xor_sync(kFull, cs, j);
+        const bool descending = (lane & k) == 0;
+        const bool keep_max = ((lane & j) == 0) == descending;
+        const bool take = keep_max ? (oc > c) : (oc < c);
+        c = take ? oc : c;
+        cs = take ? os : cs;
+      }
+    }
+    float S = 0.f;
+    for (int k = 0; k < K; ++k) S = __fadd_rn(S, __shfl_sync(kFull, cs, k));
+    if (lane < K) {
+      float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(cs, S)) : cs;
+      if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
+      const size_t o = (size_t)t * K + lane;
+      a.ids[o] = (int32_t)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
+      if (a.weights) a.weights[o] = w;
+      if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
+    }
+    return;
+  }
   if (total <= kListCap) {
     int pos = before + incl - mine;
 #pragma unroll
