@@ -16,8 +16,7 @@ size_t workspace_for(int T, int H, int E, int sm_count) {
   int S = 1, kc = 0;
   simt_plan(T, H, E, sm_count, &S, &kc);
   const size_t simt = S > 1 ? (size_t)S * T * E * sizeof(float) : 0;
-  const TcPlan p = tc_plan(T, H, E, sm_count);
-  const size_t tc = p.S > 1 ? (size_t)p.S * T * E * sizeof(float) : 0;
+  const size_t tc = tc_workspace(tc_plan(T, H, E, sm_count), T, E);
   return simt > tc ? simt : tc;
 }
 

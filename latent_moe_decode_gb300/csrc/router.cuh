@@ -15,7 +15,12 @@ struct TcPlan {
   int bn;    // token tile: 16, 32, 64, 128 or 256
   int S;     // K splits
   int n_kb;  // 64-wide K blocks
+  bool cluster;  // splits reduced on chip through distributed shared memory (no workspace)
 };
+// Split-K workspace a plan needs (bytes).
+inline size_t tc_workspace(const TcPlan& p, int T, int E) {
+  return (p.S > 1 && !p.cluster) ? (size_t)p.S * T * E * sizeof(float) : 0;
+}
 TcPlan tc_plan(int T, int H, int E, int sm_count);
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,
                      float* part, uint32_t* err, cudaStream_t stream);

@@ -58,7 +58,7 @@ extern "C" int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, f
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   const TcPlan p = tc_plan(T, H, E, dev.sm_count);
-  const size_t need = p.S > 1 ? (size_t)p.S * T * E * sizeof(float) : 0;
+  const size_t need = tc_workspace(p, T, E);
   if (need > kScratchBytes) return MOE_ERR_CAPACITY;
   float* scratch = nullptr;
   st = scratch_address(&scratch);

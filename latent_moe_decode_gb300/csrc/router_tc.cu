@@ -16,10 +16,18 @@
 //   - warp 1, one lane: issues 4 tcgen05.mma (kind::f16, BF16 x BF16 -> FP32, M=128,
 //     N=BN, K=16) per stage into a TMEM accumulator and releases the stage with
 //     tcgen05.commit on its empty mbarrier;
-//   - all 4 warps: read the accumulator back with tcgen05.ld (warp w owns TMEM lanes
-//     32w..32w+31 = 32 experts) and store FP32 rows; lanes hold consecutive experts, so
-//     every store instruction writes 128 contiguous bytes.
-// Split-K partials [S][T][E] are summed by the reduce kernel in split order.
+//   - all 16 warps: read the accumulator back with tcgen05.ld (warp w reaches TMEM lanes
+//     32(w%4)..32(w%4)+31 = 32 experts; the four warpgroups take turns on 16-column
+//     chunks) and store FP32 rows; lanes hold consecutive experts, so every store
+//     instruction writes 128 contiguous bytes. The epilogue is latency-bound, hence the
+//     many warps although the mainloop needs two threads.
+// Split-K: when the S split CTAs of a tile fit as one thread-block cluster (S <= 8,
+// all co-resident), each parks its FP32 partial tile in its own shared memory (the
+// pipeline buffers are idle by then), and after a cluster barrier every CTA sums a
+// share of the tile's token columns over the S partials -- read through distributed
+// shared memory, in split order -- and writes final logits: the partials never leave
+// the chip. Otherwise (many splits at small batches) the partials [S][T][E] go to the
+// caller's workspace and a second kernel sums them in split order.
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel sets
 // MOE_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies in flight,
 // frees its TMEM and exits.
@@ -33,7 +41,8 @@ namespace {
 
 constexpr int kBM = 128;              // experts per CTA (TMEM lanes)
 constexpr int kBK = 64;               // K elements per stage (128 bytes: one swizzle span)
-constexpr int kThreads = 128;         // 4 warps
+constexpr int kThreads = 512;         // 16 warps: two lanes run the mainloop, all sixteen the epilogue
+constexpr int kGroups = kThreads / 128;  // warpgroups: each reaches all 128 TMEM lanes
 
 template <int BN>
 struct Cfg {
@@ -84,10 +93,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
         "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int BN>
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store to the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// CLUSTER: the S split CTAs of a tile form one cluster and reduce through DSMEM.
+template <int BN, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, float* out,
                      int T, int E, int n_kb, int S, uint32_t* err) {
@@ -168,13 +190,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   // epilogue: TMEM lane = expert row, column = token
   const bool done = __all_sync(0xFFFFFFFFu, mbar_wait(accum, 0, err));  // warp-uniform for tcgen05.ld
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (done) {
-    const int e = mt * kBM + warp * 32 + lane;
+  const int wg = warp >> 2;                                    // warpgroup: its 16-column chunks
+  const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's 32 TMEM lanes
+  const int row = (warp & 3) * 32 + lane;                           // = expert row within the tile
+  if constexpr (CLUSTER) {
+    // Every CTA of the cluster owns a slice of the tile's token columns. Once all
+    // mainloops are over (the pipeline buffers are idle everywhere), each CTA pushes
+    // each column of its partial straight into the owner's receive buffer
+    // recv[split][column - first][row] with remote shared-memory stores; after a
+    // second barrier every owner sums its slice over the splits in split order.
+    const int slice = (BN + S - 1) / S;
+    const uint32_t recv = base;  // the pipeline buffers: >= S * slice * 128 * 4 bytes
+    // column -> (owner CTA, byte offset of this split's slot in the owner's buffer),
+    // with owner r holding columns [(r * BN) / S, ((r + 1) * BN) / S)
+    __shared__ uint32_t s_dst[BN];
+    __shared__ uint32_t s_owner[BN];
+    for (int c = threadIdx.x; c < BN; c += kThreads) {
+      const int r = ((c + 1) * S - 1) / BN;
+      s_owner[c] = (uint32_t)r;
+      s_dst[c] = recv + (uint32_t)((s * slice + (c - (r * BN) / S)) * kBM * 4);
+    }
+    cluster_sync();  // also orders the tables above
+    if (done) {
+#pragma unroll 1
+      for (int c0 = 16 * wg; c0 < BN; c0 += 16 * kGroups) {
+        uint32_t v[16];
+        tmem_ld16(tl + (uint32_t)c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          st_dsmem(s_dst[c0 + j] + (uint32_t)(row * 4), s_owner[c0 + j], __uint_as_float(v[j]));
+      }
+    }
+    cluster_sync();  // every partial column is in its owner's buffer
+    const float* buf = reinterpret_cast<const float*>(smem_raw + (recv - smem_u32(smem_raw)));
+    const int c_lo = (s * BN) / S, c_hi = ((s + 1) * BN) / S;
+    const int r128 = threadIdx.x & (kBM - 1);
+    const int e = mt * kBM + r128;
+    for (int c = c_lo + (threadIdx.x >> 7); c < c_hi; c += kGroups) {
+      const int jj = c - c_lo;
+      float p[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) p[q] = q < S ? buf[(q * slice + jj) * kBM + r128] : 0.0f;  // all loads first
+      float acc = p[0];
+#pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < S) acc = __fadd_rn(acc, p[q]);  // then the sum, in split order
+      const int t = nt * BN + c;
+      if (t < T && e < E) out[(size_t)t * E + e] = acc;
+    }
+  } else if (done) {
+    const int e = mt * kBM + row;
     float* dst = out + (size_t)s * T * E;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
+    for (int c0 = 16 * wg; c0 < BN; c0 += 16 * kGroups) {
       uint32_t v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+      tmem_ld16(tl + (uint32_t)c0, v);
+      tmem_wait_ld();
       if (e < E) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -216,17 +288,70 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool CLUSTER>
 int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, int T, int H, int E, const TcPlan& p, uint32_t* err,
               cudaStream_t stream) {
   CUtensorMap tm_w, tm_x;
   if (!make_map(&tm_w, w, E, H, kBM) || !make_map(&tm_x, x, T, H, BN)) return MOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(router_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem) !=
-      cudaSuccess)
+  auto kern = router_tc_kernel<BN, CLUSTER>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem) != cudaSuccess)
     return MOE_ERR_CUDA;
-  dim3 grid(p.S, (T + BN - 1) / BN, (E + kBM - 1) / kBM);
-  return launch_pdl(router_tc_kernel<BN>, grid, dim3(kThreads), Cfg<BN>::kSmem, stream, tm_w, tm_x, dst, T, E, p.n_kb,
-                    p.S, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.S, (T + BN - 1) / BN, (E + kBM - 1) / kBM);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<BN>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CLUSTER ? p.S : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CLUSTER ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, dst, T, E, p.n_kb, p.S, err) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Clusters of S split CTAs (one tile each) that can be resident at once.
+template <int BN>
+int max_clusters(int S) {
+  static int cache[9] = {0};
+  if (S < 2 || S > 8) return 0;
+  if (cache[S]) return cache[S];
+  auto kern = router_tc_kernel<BN, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, 64, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<BN>::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[S] = n > 0 ? n : -1;
+  return n;
+}
+
+int max_clusters_bn(int bn, int S) {
+  switch (bn) {
+    case 16: return max_clusters<16>(S);
+    case 32: return max_clusters<32>(S);
+    case 64: return max_clusters<64>(S);
+    case 128: return max_clusters<128>(S);
+    default: return max_clusters<256>(S);
+  }
 }
 
 }  // namespace
@@ -246,21 +371,42 @@ TcPlan tc_plan(int T, int H, int E, int sm_count) {
   s = s > 32 ? 32 : s;
   if (s > p.n_kb / 2) s = p.n_kb / 2 > 0 ? p.n_kb / 2 : 1;
   p.S = s;
+  p.cluster = false;
+  if (s >= 2 && s <= 8) {
+    // the largest cluster of splits whose clusters are all resident at once
+    for (int c = s; c >= 2; --c) {
+      if (max_clusters_bn(p.bn, c) >= tiles) {
+        p.S = c;
+        p.cluster = true;
+        break;
+      }
+    }
+  }
   return p;
 }
 
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,
                      float* part, uint32_t* err, cudaStream_t stream) {
-  float* dst = p.S == 1 ? logits : part;
+  const bool direct = p.S == 1 || p.cluster;
+  float* dst = direct ? logits : part;
   int st;
+#define MOE_TC_CASE(B)                                                                                   \
+  case B:                                                                                                 \
+    st = p.cluster ? launch_bn<B, true>(x, w, dst, T, H, E, p, err, stream)                             \
+                   : launch_bn<B, false>(x, w, dst, T, H, E, p, err, stream);                            \
+    break;
   switch (p.bn) {
-    case 16: st = launch_bn<16>(x, w, dst, T, H, E, p, err, stream); break;
-    case 32: st = launch_bn<32>(x, w, dst, T, H, E, p, err, stream); break;
-    case 64: st = launch_bn<64>(x, w, dst, T, H, E, p, err, stream); break;
-    case 128: st = launch_bn<128>(x, w, dst, T, H, E, p, err, stream); break;
-    default: st = launch_bn<256>(x, w, dst, T, H, E, p, err, stream); break;
+    MOE_TC_CASE(16)
+    MOE_TC_CASE(32)
+    MOE_TC_CASE(64)
+    MOE_TC_CASE(128)
+    default:
+      st = p.cluster ? launch_bn<256, true>(x, w, dst, T, H, E, p, err, stream)
+                     : launch_bn<256, false>(x, w, dst, T, H, E, p, err, stream);
+      break;
   }
-  if (st != MOE_OK || p.S == 1) return st;
+#undef MOE_TC_CASE
+  if (st != MOE_OK || direct) return st;
   return launch_router_reduce(part, p.S, T, E, logits, stream);
 }
 
