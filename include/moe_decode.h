@@ -162,6 +162,16 @@ int moe_topk_route(const float* logits, const float* bias, int T, int E, int K, 
                    float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,
                    moe_stream_t stream);
 
+/* moe_topk_route and mxfp8_quantize_rows(latent, rows, cols, q, scales) in ONE launch
+ * ([wide] WideRoute: one launch of 2b CTAs, CTA t routes token t, CTA b + t writes the
+ * MXFP8 plan row of token t): the quantisation CTAs stream the latent on the SMs the
+ * selection leaves free. Results are identical to the two separate calls; arguments
+ * and requirements are theirs (T >= 1; rows may be 0). */
+int moe_topk_route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize,
+                            float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,
+                            const uint16_t* latent, int rows, int cols, uint8_t* q, uint8_t* scales,
+                            moe_stream_t stream);
+
 /* -------------------------------------------------------------------------------
  * Per-expert routing lists (counting sort, CSR).
  * Source: [wide] WideRoute docstring and kernel: each of token t's K (token, slot)

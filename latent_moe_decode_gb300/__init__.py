@@ -40,6 +40,7 @@ SIGNATURES = {
     "moe_router_logits_ex": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _I, _P]),
     "moe_router_logits_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "moe_topk_route_quantize": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "moe_build_routing_lists_workspace": (_SZ, [_I, _I, _I]),
     "moe_build_routing_lists": (_I, [_P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -145,6 +146,27 @@ def topk_route(logits, bias, K: int, renormalize: bool = True, scale: float = 1.
     return ids, weights, weights_bf16
 
 
+def topk_route_quantize(logits, bias, K: int, latent, renormalize: bool = True, scale: float = 1.0, ids=None,
+                        weights=None, weights_bf16=None, q=None, scales=None, stream=None):
+    """topk_route and mxfp8_quantize_rows(latent) in one launch:
+    (ids, weights, weights_bf16, q, scales)."""
+    T, E = logits.shape
+    _need(logits, torch.float32, (T, E), "logits")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    rows, cols = latent.shape
+    _need(latent, torch.bfloat16, (rows, cols), "latent")
+    ids = _empty((T, K), torch.int32, logits) if ids is None else _need(ids, torch.int32, (T, K), "ids")
+    weights = _empty((T, K), torch.float32, logits) if weights is None else _need(weights, torch.float32, (T, K), "weights")
+    weights_bf16 = _empty((T, K), torch.bfloat16, logits) if weights_bf16 is None else _need(weights_bf16, torch.bfloat16, (T, K), "weights_bf16")
+    q = _empty((rows, cols), torch.uint8, latent) if q is None else _need(q, torch.uint8, (rows, cols), "q")
+    scales = _empty((rows, cols // 32), torch.uint8, latent) if scales is None else _need(scales, torch.uint8, (rows, cols // 32), "scales")
+    _check("moe_topk_route_quantize", load().moe_topk_route_quantize(
+        _ptr(logits), _ptr(bias), T, E, K, int(bool(renormalize)), float(scale), _ptr(ids), _ptr(weights),
+        _ptr(weights_bf16), _ptr(latent), rows, cols, _ptr(q), _ptr(scales), _stream(stream)))
+    return ids, weights, weights_bf16, q, scales
+
+
 def build_routing_lists_workspace(T: int, K: int, E: int) -> int:
     return int(load().moe_build_routing_lists_workspace(T, K, E))
 
@@ -205,11 +227,14 @@ def device_error(clear: bool = True) -> int:
 
 
 class RouteFinalize:
-    """The whole routing-and-combine step on one stream, with its buffers preallocated:
-    router logits -> sigmoid+bias top-K -> routing lists -> MXFP8 latent -> Finalize.
+    """The whole routing-and-combine step, with its buffers preallocated:
+    router logits -> sigmoid+bias top-K with the MXFP8 latent in the same launch ->
+    Finalize, and the routing lists on a side stream beside Finalize (Finalize does
+    not read them).
 
-    ``run()`` launches the library's kernels back to back (programmatic dependent
-    launch between them) and allocates nothing, so it can be captured in a CUDA graph.
+    ``run()`` launches the library's kernels (programmatic dependent launch between
+    consecutive kernels of a stream) and allocates nothing, so it can be captured in a
+    CUDA graph.
     """
 
     def __init__(self, T: int, H: int, L: int, E: int, K: int, device="cuda", renormalize=True, scale=1.0,
@@ -229,19 +254,23 @@ class RouteFinalize:
         self.out = e((T, L), torch.bfloat16)
         self.router_ws = e((max(1, router_logits_workspace(T, H, E)),), torch.uint8)
         self.lists_ws = e((max(1, build_routing_lists_workspace(T, K, E)),), torch.uint8)
+        self.side = torch.cuda.Stream(dev)
         self.launches = self._count_launches()
 
     def _count_launches(self) -> int:
         """Kernels one run() launches."""
-        # router (+ its split-K reduce when it needs scratch), top-k, lists, MXFP8, Finalize
-        return 5 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0)
+        # router (+ its split-K reduce when it needs scratch), top-k + MXFP8, lists, Finalize
+        return 4 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0)
 
     def run(self, x, w, bias, latent, rows, stream=None):
-        router_logits(x, w, out=self.logits, workspace=self.router_ws, algo=self.router_algo, stream=stream)
-        topk_route(self.logits, bias, self.K, self.renormalize, self.scale, ids=self.ids, weights=self.weights,
-                   weights_bf16=self.weights_bf16, stream=stream)
+        main = stream if stream is not None else torch.cuda.current_stream()
+        router_logits(x, w, out=self.logits, workspace=self.router_ws, algo=self.router_algo, stream=main)
+        topk_route_quantize(self.logits, bias, self.K, latent, self.renormalize, self.scale, ids=self.ids,
+                            weights=self.weights, weights_bf16=self.weights_bf16, q=self.q, scales=self.scales,
+                            stream=main)
+        self.side.wait_stream(main)
         build_routing_lists(self.ids, self.E, offsets=self.offsets, pairs=self.pairs, workspace=self.lists_ws,
-                            stream=stream)
-        mxfp8_quantize_rows(latent, q=self.q, scales=self.scales, stream=stream)
-        finalize(rows, self.weights_bf16, self.T, self.K, out=self.out, stream=stream)
+                            stream=self.side)
+        finalize(rows, self.weights_bf16, self.T, self.K, out=self.out, stream=main)
+        main.wait_stream(self.side)
         return self.out

@@ -26,7 +26,8 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxEpc = 32;  // experts per CTA
+constexpr int kMaxEpc = 32;      // experts per CTA
+constexpr int kTargetCtas = 32;  // CTAs per launch (E / kMaxEpc at most 32 for E <= 1024)
 constexpr int kBatch = 8;   // int4 loads in flight per lane (1024 ids per warp per batch)
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -174,7 +175,9 @@ extern "C" int moe_build_routing_lists(const int32_t* ids, int T, int K, int E, 
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
-  int epc = (E + dev.sm_count - 1) / dev.sm_count;
+  // The time is set by each CTA's scan of all ids, not by the CTA count, so few CTAs
+  // (about 32) do: the rest of the GPU stays free for work running beside the lists.
+  int epc = (E + kTargetCtas - 1) / kTargetCtas;
   epc = epc < 1 ? 1 : (epc > kMaxEpc ? kMaxEpc : epc);
   const long long n = (long long)T * K;
   ListArgs a{ids, n, E, epc, offsets, pairs, dev.error_word, (K % 4 == 0 && aligned(ids, 16)) ? 1 : 0};

@@ -1,0 +1,95 @@
+// MXFP8 (OCP MX) quantisation of a flat BF16 span: the per-CTA body shared by the
+// quantisation kernel and the fused top-K + MXFP8 launch.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace mxfp8_impl {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One CTA's 16-byte chunks [block * THREADS * UNROLL, ...) of the flat input.
+template <int THREADS, int UNROLL>
+__device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long long nchunks, uint8_t* __restrict__ q,
+                                            uint8_t* __restrict__ scales, uint32_t* err, long long block) {
+  constexpr int kThreads = THREADS, kUnroll = UNROLL;
+  __shared__ __align__(128) uint4 stage[kThreads * kUnroll];
+  __shared__ __align__(8) uint64_t bar_mem;
+  const int lane = threadIdx.x & 31;
+  const long long cta0 = block * kThreads * kUnroll;  // first chunk of this CTA
+  const int nch = (int)min((long long)kThreads * kUnroll, nchunks - cta0);
+  const uint32_t bar = smem_u32(&bar_mem);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();  // the barrier is initialised before any thread waits on it
+  grid_launch_dependents();
+  grid_wait();
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar, (uint32_t)nch * 16u);
+    bulk_g2s(smem_u32(stage), x + cta0 * 8, (uint32_t)nch * 16u, bar, policy_evict_first());
+  }
+  const bool ok = __all_sync(kFullMask, mbar_wait(bar, 0, err));
+  if (!ok) return;
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int wl = u * kThreads + (threadIdx.x & ~31);  // this warp's first chunk in the CTA
+    if (wl >= nch) break;                                // warp-uniform
+    const int cl = wl + lane;
+    const uint4 v = cl < nch ? stage[cl] : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    m = max(m, __shfl_xor_sync(kFullMask, m, 1));
+    m = max(m, __shfl_xor_sync(kFullMask, m, 2));
+    uint32_t sbyte;
+    uint2 codes;
+    if (m >= 0x7F80u) {  // an infinity or NaN in the block
+      sbyte = 0xFFu;
+      codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    } else {
+      int se = -127;
+      if (m != 0u) {
+        const int ex = (int)(m >> 7);
+        const int fl = ex ? ex - 127 : (31 - __clz((int)(m & 0x7Fu))) - 133;
+        se = min(max(fl - 8, -127), 127);
+      }
+      sbyte = (uint32_t)(se + 127);
+      const float mult = __int_as_float((127 - se) << 23);  // 2^-se, a normal FP32
+      uint32_t p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p[j] = e4m3x2(__fmul_rn(bf16_lo(w[j]), mult), __fmul_rn(bf16_hi(w[j]), mult));
+      codes = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+    }
+    const long long c = cta0 + cl;
+    if (cl < nch) *reinterpret_cast<uint2*>(q + c * 8) = codes;
+    // scale bytes of the warp's 8 blocks (held by lanes 0, 4, ..., 28)
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = __shfl_sync(kFullMask, sbyte, 4 * i);
+    const long long blk0 = (cta0 + wl) >> 2;
+    if (lane == 0) {
+      if (wl + 32 <= nch) {
+        *reinterpret_cast<uint2*>(scales + blk0) =
+            make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+      } else {
+        const int nb = (nch - wl) >> 2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < nb) scales[blk0 + i] = (uint8_t)b[i];
+      }
+    }
+  }
+}
+
+}  // namespace mxfp8_impl
+}  // namespace moe

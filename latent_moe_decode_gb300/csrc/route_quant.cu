@@ -1,0 +1,74 @@
+// Sigmoid + bias top-K and MXFP8 quantisation of the latent rows in one launch.
+//
+// Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideRoute:
+// one launch of 2b CTAs in which CTA t routes token t and CTA b + t writes token t's
+// MXFP8 plan row from the BF16 latent.
+//
+// GB300 design: the two jobs share nothing, so in one grid the quantisation CTAs
+// stream the latent through HBM on the SMs the routing CTAs leave free, instead of
+// running after them. CTAs [0, T) run the top-K selection of token t (topk.cuh);
+// CTAs [T, T + Q) each quantise a 16 KB span of the latent (mxfp8.cuh), one bulk copy
+// per CTA. Both bodies are the ones the separate calls use, so the results are
+// identical to moe_topk_route followed by mxfp8_quantize_rows.
+#include "mxfp8.cuh"
+#include "topk.cuh"
+
+namespace moe {
+namespace {
+
+using namespace topk_impl;
+constexpr int kQuantUnroll = 8;  // 128 threads x 8 chunks = 16 KB per quantisation CTA
+
+template <int NJ>
+__global__ void __launch_bounds__(kThreads) route_quant_kernel(const TopkArgs a, const uint16_t* __restrict__ x,
+                                                               long long nchunks, uint8_t* __restrict__ q,
+                                                               uint8_t* __restrict__ scales, uint32_t* err) {
+  if ((int)blockIdx.x < a.T)
+    topk_token<NJ>(a, (int)blockIdx.x);
+  else
+    mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)blockIdx.x - a.T);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_topk_route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize,
+                                       float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,
+                                       const uint16_t* latent, int rows, int cols, uint8_t* q, uint8_t* scales,
+                                       moe_stream_t stream) {
+  using namespace moe;
+  using namespace moe::topk_impl;
+  if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARGUMENT;
+  if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK) return MOE_ERR_CAPACITY;
+  if (rows < 0 || cols < 32 || cols % 32 != 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (!logits || !ids || (rows > 0 && (!latent || !q || !scales))) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(logits, 4) || (bias && !aligned(bias, 4)) || !aligned(ids, 4) || (weights && !aligned(weights, 4)) ||
+      (weights_bf16 && !aligned(weights_bf16, 2)))
+    return MOE_ERR_ALIGNMENT;
+  if (rows > 0 && (!aligned(latent, 16) || !aligned(q, 8) || !aligned(scales, 8))) return MOE_ERR_ALIGNMENT;
+  const long long nchunks = (long long)rows * (cols / 8);
+  const long long per = (long long)kThreads * kQuantUnroll;
+  const long long qblocks = (nchunks + per - 1) / per;
+  if ((long long)T + qblocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != MOE_OK) return st;
+  TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
+  const dim3 grid((unsigned)(T + qblocks)), block(kThreads);
+  cudaStream_t s = as_cuda(stream);
+  switch ((E + 127) / 128) {
+#define MOE_RQ_CASE(N) \
+  case N:              \
+    return launch_pdl(route_quant_kernel<N>, grid, block, 0, s, a, latent, nchunks, q, scales, dev.error_word);
+    MOE_RQ_CASE(1)
+    MOE_RQ_CASE(2)
+    MOE_RQ_CASE(3)
+    MOE_RQ_CASE(4)
+    MOE_RQ_CASE(5)
+    MOE_RQ_CASE(6)
+    MOE_RQ_CASE(7)
+    MOE_RQ_CASE(8)
+#undef MOE_RQ_CASE
+  }
+  return MOE_ERR_CAPACITY;
+}

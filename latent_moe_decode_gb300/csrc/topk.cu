@@ -19,311 +19,27 @@
 // up to 32 of them are ordered by one warp-wide bitonic sort of (key, ~expert), so
 // lane k holds slot k (32 < count <= 64: ranked by counting; more, from heavy ties:
 // K rounds of argmax).
-#include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kListCap = 64;
-constexpr unsigned kFull = 0xFFFFFFFFu;
-
-// --- the specified sigmoid -------------------------------------------------------
-// exp(y) = 2^n exp(r), n = rint(y log2 e), r = y - n ln2 with ln2 split into a high
-// part whose low 12 significand bits are zero (so n * LN2_HI is exact) and a low part
-// (Cody & Waite, 1980); exp(r) by the degree-7 Taylor polynomial in Horner form with
-// fused multiply-adds; 2^n applied as two exact power-of-two products.
-constexpr double kLn2 = 0.693147180559945309417232121458;
-constexpr float kLog2e = (float)(1.0 / kLn2);
-constexpr float kLn2Hi = 0.693115234375f;  // (float)ln2 = 0x3F317218 with the low 12 bits cleared
-constexpr float kLn2Lo = (float)(kLn2 - 0.693115234375);
-constexpr float kC0 = 1.0f, kC1 = 1.0f, kC2 = (float)(1.0 / 2.0), kC3 = (float)(1.0 / 6.0),
-                kC4 = (float)(1.0 / 24.0), kC5 = (float)(1.0 / 120.0), kC6 = (float)(1.0 / 720.0),
-                kC7 = (float)(1.0 / 5040.0);
-
-__device__ __forceinline__ float round_half_even(float x) {
-  float r;
-  asm("cvt.rni.f32.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-__device__ __forceinline__ float spec_exp(float y) {  // -17.5 < y < 88.5
-  const float n = round_half_even(__fmul_rn(y, kLog2e));
-  float r = __fmaf_rn(-n, kLn2Hi, y);
-  r = __fmaf_rn(-n, kLn2Lo, r);
-  float p = kC7;
-  p = __fmaf_rn(p, r, kC6);
-  p = __fmaf_rn(p, r, kC5);
-  p = __fmaf_rn(p, r, kC4);
-  p = __fmaf_rn(p, r, kC3);
-  p = __fmaf_rn(p, r, kC2);
-  p = __fmaf_rn(p, r, kC1);
-  p = __fmaf_rn(p, r, kC0);
-  const int ni = (int)n;
-  const int a = ni / 2, b = ni - a;
-  p = __fmul_rn(p, __int_as_float((a + 127) << 23));
-  p = __fmul_rn(p, __int_as_float((b + 127) << 23));
-  return p;
-}
-
-// sigma(x) = 1 / (1 + exp(-x)), correctly rounded reciprocal; 1 for x >= 17.5,
-// 0 for x <= -88.5, NaN for NaN (special cases selected, not branched).
-__device__ __forceinline__ float spec_sigmoid(float x) {
-  const bool hi = x >= 17.5f, lo = x <= -88.5f;
-  const float e = spec_exp((hi || lo) ? 0.0f : -x);
-  const float r = __frcp_rn(__fadd_rn(1.0f, e));
-  return hi ? 1.0f : (lo ? 0.0f : r);
-}
-
-// Monotone 32-bit key of an FP32 value: larger value -> larger key, -0 == +0,
-// NaN -> 1 (below every number); 0 is reserved for "no candidate".
-__device__ __forceinline__ uint32_t order_key(float c) {
-  if (c != c) return 1u;
-  uint32_t b = __float_as_uint(c);
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-struct TopkArgs {
-  const float* logits;
-  const float* bias;
-  int T, E, K, renorm;
-  float scale;
-  int32_t* ids;
-  float* weights;
-  uint16_t* weights_bf16;
-};
-
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
+using namespace topk_impl;
 
 template <int NJ>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
-  __shared__ uint32_t s_top[kWarps][32];
-  __shared__ int s_cnt[kWarps];
-  __shared__ uint32_t l_key[kListCap];
-  __shared__ int32_t l_e[kListCap];
-  __shared__ float l_s[kListCap];
-  __shared__ int32_t slot_id[MOE_MAX_TOPK];
-  __shared__ float slot_s[MOE_MAX_TOPK];
-  __shared__ uint32_t r_key[kWarps];
-  __shared__ int32_t r_e[kWarps];
-  __shared__ float r_s[kWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = blockIdx.x;
-  const int E = a.E, K = a.K;
-  grid_launch_dependents();
-  grid_wait();
-  const float* lg = a.logits + (size_t)t * E;
-
-  // 1) scores and keys of this thread's experts tid + 128 j
-  uint32_t key[NJ];
-  float s[NJ];
-  float x[NJ], b[NJ];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int e = tid + 128 * j;
-    x[j] = e < E ? __ldg(lg + e) : 0.f;
-    b[j] = (a.bias && e < E) ? __ldg(a.bias + e) : 0.f;
-  }
-  uint32_t tmax = 0;
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int e = tid + 128 * j;
-    const float sv = spec_sigmoid(x[j]);
-    const float c = a.bias ? __fadd_rn(sv, b[j]) : sv;
-    s[j] = sv;
-    key[j] = e < E ? order_key(c) : 0u;
-    tmax = max(tmax, key[j]);
-  }
-
-  // 2) bound: the K-th largest of the 128 thread maxima
-  uint32_t v = tmax;
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint32_t o = __shfl_xor_sync(kFull, v, j);
-      const bool descending = (lane & k) == 0;
-      const bool keep_max = ((lane & j) == 0) == descending;
-      v = keep_max ? max(v, o) : min(v, o);
-    }
-  }
-  s_top[warp][lane] = v;  // descending: lane l holds the warp's (l+1)-th largest
-  __syncthreads();
-  // top 32 of the union of two descending lists: max(a[l], b[31-l]) is bitonic;
-  // five half-cleaner steps sort it descending
-  auto merge = [&](uint32_t x, uint32_t y) {
-    uint32_t m = max(x, y);
-#pragma unroll
-    for (int j = 16; j > 0; j >>= 1) {
-      const uint32_t o = __shfl_xor_sync(kFull, m, j);
-      m = (lane & j) == 0 ? max(m, o) : min(m, o);
-    }
-    return m;
-  };
-  const uint32_t m01 = merge(s_top[0][lane], s_top[1][31 - lane]);
-  const uint32_t m23 = merge(s_top[2][lane], s_top[3][31 - lane]);
-  const uint32_t top = merge(m01, __shfl_sync(kFull, m23, 31 - lane));
-  const uint32_t bound = __shfl_sync(kFull, top, K - 1);
-
-  // 3) candidates at or above the bound, compacted in thread order
-  uint32_t flags = 0;
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (key[j] != 0u && key[j] >= bound) flags |= 1u << j;
-  const int mine = __popc(flags);
-  int incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_cnt[warp] = incl;
-  __syncthreads();
-  int before = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    before += w < warp ? s_cnt[w] : 0;
-    total += s_cnt[w];
-  }
-
-  if (total <= 32) {
-    // compact, then one warp sorts (key desc, expert asc): lane k holds slot k
-    int pos = before + incl - mine;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (flags & (1u << j)) {
-        l_key[pos] = key[j];
-        l_e[pos] = tid + 128 * j;
-        l_s[pos] = s[j];
-        ++pos;
-      }
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    unsigned long long c = 0;  // (key << 32) | ~expert; 0 = empty
-    float cs = 0.f;
-    if (lane < total) {
-      c = ((unsigned long long)l_key[lane] << 32) | (0xFFFFFFFFu - (uint32_t)l_e[lane]);
-      cs = l_s[lane];
-    }
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const unsigned long long oc = __shfl_xor_sync(kFull, c, j);
-        const float os = __shfl_xor_sync(kFull, cs, j);
-        const bool descending = (lane & k) == 0;
-        const bool keep_max = ((lane & j) == 0) == descending;
-        const bool take = keep_max ? (oc > c) : (oc < c);
-        c = take ? oc : c;
-        cs = take ? os : cs;
-      }
-    }
-    float S = 0.f;
-    for (int k = 0; k < K; ++k) S = __fadd_rn(S, __shfl_sync(kFull, cs, k));
-    if (lane < K) {
-      float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(cs, S)) : cs;
-      if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
-      const size_t o = (size_t)t * K + lane;
-      a.ids[o] = (int32_t)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
-      if (a.weights) a.weights[o] = w;
-      if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
-    }
-    return;
-  }
-  if (total <= kListCap) {
-    int pos = before + incl - mine;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (flags & (1u << j)) {
-        l_key[pos] = key[j];
-        l_e[pos] = tid + 128 * j;
-        l_s[pos] = s[j];
-        ++pos;
-      }
-    }
-    __syncthreads();
-    if (tid < total) {
-      const uint32_t ki = l_key[tid];
-      const int ei = l_e[tid];
-      int rank = 0;
-      for (int q = 0; q < total; ++q) {
-        const uint32_t kq = l_key[q];
-        rank += (kq > ki) || (kq == ki && l_e[q] < ei);
-      }
-      if (rank < K) {
-        slot_id[rank] = ei;
-        slot_s[rank] = l_s[tid];
-      }
-    }
-  } else {
-    // heavy ties: K rounds of argmax over (key desc, expert asc)
-    for (int k = 0; k < K; ++k) {
-      uint32_t bk = 0;
-      int be = 0x7FFFFFFF;
-      float bs = 0.f;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        if (key[j] > bk) {  // ascending expert order within the thread: first max wins
-          bk = key[j];
-          be = tid + 128 * j;
-          bs = s[j];
-        }
-      }
-      const uint32_t wk = __reduce_max_sync(kFull, bk);
-      const int we = (int)__reduce_min_sync(kFull, bk == wk ? (uint32_t)be : 0x7FFFFFFFu);
-      const float ws = __shfl_sync(kFull, bs, we & 31);  // expert e lives in thread e % 128
-      if (lane == 0) {
-        r_key[warp] = wk;
-        r_e[warp] = we;
-        r_s[warp] = ws;
-      }
-      __syncthreads();
-      uint32_t gk = 0;
-      int ge = 0x7FFFFFFF;
-      float gs = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        if (r_key[w] > gk || (r_key[w] == gk && r_e[w] < ge)) {
-          gk = r_key[w];
-          ge = r_e[w];
-          gs = r_s[w];
-        }
-      }
-      if (tid == 0) {
-        slot_id[k] = ge;
-        slot_s[k] = gs;
-      }
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if (tid + 128 * j == ge) key[j] = 0u;
-      __syncthreads();
-    }
-  }
-  __syncthreads();
-
-  // 4) weights: unbiased scores over their slot-order FP32 sum
-  if (tid < K) {
-    float S = 0.f;
-    for (int k = 0; k < K; ++k) S = __fadd_rn(S, slot_s[k]);
-    const float sv = slot_s[tid];
-    float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(sv, S)) : sv;
-    if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
-    const size_t o = (size_t)t * K + tid;
-    a.ids[o] = slot_id[tid];
-    if (a.weights) a.weights[o] = w;
-    if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
-  }
+  topk_token<NJ>(a, blockIdx.x);
 }
 
 }  // namespace
 }  // namespace moe
 
+
 extern "C" int moe_topk_route(const float* logits, const float* bias, int T, int E, int K,
                               int renormalize, float scale, int32_t* ids, float* weights,
                               uint16_t* weights_bf16, moe_stream_t stream) {
   using namespace moe;
+  using namespace moe::topk_impl;
   if (T < 0 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARGUMENT;
   if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK) return MOE_ERR_CAPACITY;
   if (T == 0) return MOE_OK;

@@ -83,3 +83,22 @@ def test_sigmoid_exhaustive(moe, orc):
             exp = np.concatenate(list(ex.map(orc.sigmoid, parts)))
         same = (got.view(np.uint32) == exp.view(np.uint32)) | (np.isnan(got) & np.isnan(exp))
         assert same.all(), f"mismatch at 0x{int(u[~same][0]):08x}"
+
+
+@pytest.mark.parametrize("T,rows", [(1020, 1020), (8, 8), (37, 5), (3, 0)])
+def test_fused_route_quantize(moe, orc, T, rows):
+    """moe_topk_route_quantize == moe_topk_route + mxfp8_quantize_rows, bit for bit."""
+    logits = synth.normal_f32(26 + T, 1, (T, 896), 1.7)
+    bias = synth.correction_bias()
+    latent = synth.latent_rows(max(rows, 1))[:rows]
+    from gpu_helpers import bf16_dev
+    ids, w, wb, q, sc = moe.topk_route_quantize(dev(logits), dev(bias), 16, bf16_dev(latent))
+    torch.cuda.synchronize()
+    eids, ew, ewb = orc.topk_route(logits, bias, 16)
+    np.testing.assert_array_equal(host(ids), eids)
+    np.testing.assert_array_equal(host(w).view(np.uint32), ew.view(np.uint32))
+    np.testing.assert_array_equal(bf16_bits(wb), ewb)
+    if rows:
+        eq, es = orc.mxfp8_quantize(latent)
+        np.testing.assert_array_equal(host(q), eq)
+        np.testing.assert_array_equal(host(sc), es)
