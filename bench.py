@@ -183,6 +183,16 @@ class Step:
 SLEEP_CYCLES = 200_000  # ~100 us of GPU spin so the host is ahead when the timed work starts
 
 
+def flush_l2(flush, i):
+    """Writes the 256 MB buffer (evicting everything), then reads it back, so the dirty
+    lines of the write are written back here and the timed kernels start on a cold,
+    clean L2 (as a profiler's cache flush leaves it)."""
+    import torch
+
+    flush.fill_(i & 0xFF)
+    torch.sum(flush.view(torch.int64))
+
+
 def time_region(fn, n, flush, stream):
     """CUDA-event times of fn() over n repetitions; before each one L2 is flushed and
     the GPU spins briefly (both outside the events) so the launch is already queued."""
@@ -190,7 +200,7 @@ def time_region(fn, n, flush, stream):
 
     evs = []
     for i in range(n):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, i)
         torch.cuda._sleep(SLEEP_CYCLES)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -297,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the pages' wide decode batch)",
         "config": {"workload": WORKLOAD, "T": T, "hidden": synth.H, "latent": synth.L, "experts": synth.E, "top_k": synth.K,
-                   "l2": "flushed (256 MB write) before every timed step, outside its events",
+                   "l2": "flushed before every timed step, outside its events: 256 MB written, then read back (cold, clean L2)",
                    "launch": "the step's kernels captured once in a CUDA graph, programmatic dependent launch between them",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "chain_GB/s": round(chain_bytes(ab) / (ms * 1e-3) / 1e9, 1),
