@@ -154,8 +154,9 @@ int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, float* logit
  *   ids          device, int32 [T, K]   output
  *   weights      device, FP32 [T, K]    output (may be NULL)
  *   weights_bf16 device, BF16 [T, K]    output (may be NULL)
- * Requirements: T >= 1, 1 <= K <= min(E, MOE_MAX_TOPK), 1 <= E <= MOE_MAX_EXPERTS
- * (MOE_ERR_CAPACITY beyond), logits 16-byte aligned when E % 4 == 0.
+ * Requirements: T >= 0 (T == 0 launches nothing), 1 <= K <= min(E, MOE_MAX_TOPK),
+ * 1 <= E <= MOE_MAX_EXPERTS (MOE_ERR_CAPACITY beyond); logits, bias, ids and weights
+ * 4-byte aligned, weights_bf16 2-byte aligned (MOE_ERR_ALIGNMENT otherwise).
  * Bit-exact and deterministic.
  * ------------------------------------------------------------------------------- */
 int moe_topk_route(const float* logits, const float* bias, int T, int E, int K, int renormalize,
@@ -182,13 +183,13 @@ int moe_topk_route_quantize(const float* logits, const float* bias, int T, int E
  *   ascending t (so ascending code). offsets = exclusive prefix sum of the per-expert
  *   counts; offsets[0] = 0, offsets[E] = T*K.
  *
- *   ids       device, int32 [T, K]   (within a row the ids must be distinct)
+ *   ids       device, int32 [T, K]   (an id may repeat within a row: each pair is listed)
  *   offsets   device, int32 [E + 1]  output
  *   pairs     device, int32 [T * K]  output
- *   workspace device scratch of moe_build_routing_lists_workspace(T, K, E) bytes (0 for
- *             T <= 1024: then NULL is fine); clobbered.
+ *   workspace device scratch of moe_build_routing_lists_workspace(T, K, E) bytes; that
+ *             size is 0 (NULL is fine): the lists need no scratch.
  * Requirements: T >= 0 (T == 0 writes offsets = 0), 1 <= K <= MOE_MAX_TOPK,
- * 1 <= E <= MOE_MAX_EXPERTS, ids 16-byte aligned when K % 4 == 0.
+ * 1 <= E <= MOE_MAX_EXPERTS, T*K < 2^31; ids, offsets and pairs 4-byte aligned.
  * An id outside [0, E) is dropped and sets MOE_DEVERR_EXPERT_ID (the lists are then
  * incomplete). Deterministic and free of global atomics.
  * ------------------------------------------------------------------------------- */

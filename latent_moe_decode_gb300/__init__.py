@@ -229,8 +229,9 @@ def device_error(clear: bool = True) -> int:
 class RouteFinalize:
     """The whole routing-and-combine step, with its buffers preallocated:
     router logits -> sigmoid+bias top-K with the MXFP8 latent in the same launch ->
-    Finalize, and the routing lists on a side stream beside Finalize (Finalize does
-    not read them).
+    routing lists -> Finalize, on one stream. (Finalize does not read the lists, but
+    beside it the lists kernel, latency-bound, waits behind Finalize's HBM stream and
+    leaves Finalize's SMs unevenly loaded: in sequence the step is shorter.)
 
     ``run()`` launches the library's kernels (programmatic dependent launch between
     consecutive kernels of a stream) and allocates nothing, so it can be captured in a
@@ -254,7 +255,6 @@ class RouteFinalize:
         self.out = e((T, L), torch.bfloat16)
         self.router_ws = e((max(1, router_logits_workspace(T, H, E)),), torch.uint8)
         self.lists_ws = e((max(1, build_routing_lists_workspace(T, K, E)),), torch.uint8)
-        self.side = torch.cuda.Stream(dev)
         self.launches = self._count_launches()
 
     def _count_launches(self) -> int:
@@ -268,9 +268,7 @@ class RouteFinalize:
         topk_route_quantize(self.logits, bias, self.K, latent, self.renormalize, self.scale, ids=self.ids,
                             weights=self.weights, weights_bf16=self.weights_bf16, q=self.q, scales=self.scales,
                             stream=main)
-        self.side.wait_stream(main)
         build_routing_lists(self.ids, self.E, offsets=self.offsets, pairs=self.pairs, workspace=self.lists_ws,
-                            stream=self.side)
+                            stream=main)
         finalize(rows, self.weights_bf16, self.T, self.K, out=self.out, stream=main)
-        main.wait_stream(self.side)
         return self.out

@@ -20,6 +20,12 @@ struct DeviceInfo {
 // Facts about the current device, cached per device. Returns MOE_OK or an error.
 int current_device(DeviceInfo* out);
 
+// Every kernel of the library runs with the largest shared-memory carveout (once per
+// kernel and device). The kernels of one step then share one SM configuration: an SM
+// need not drain to switch its L1/shared split between them, so a kernel can start
+// beside, or (programmatic dependent launch) right behind, the previous one.
+int prefer_max_shared(const void* func);
+
 inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -30,6 +36,7 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 template <typename... KArgs, typename... Args>
 int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                Args&&... args) {
+  if (prefer_max_shared(reinterpret_cast<const void*>(kernel)) != MOE_OK) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;

@@ -8,16 +8,23 @@
 // when it is not 1, zero for a -1 permuted index whose row is skipped; the
 // shared-expert row added once in FP32 after all k).
 //
-// GB300 design: a pure HBM stream (T*K rows of H BF16 in, T rows out). One thread owns
-// one 16-byte fragment (8 columns) of one token; the grid is flat over (token,
-// fragment), so a warp covers 512 contiguous bytes of each row. The thread issues the
-// asynchronous 16-byte copies (cp.async, bypassing L1, evict-first in L2) of all of its
-// K row fragments into its own shared-memory slots before it touches any of them, so
-// all K loads are in flight at once whatever registers the compiler allocates
-// (16 x 16 B per thread, ~220 KB per SM at 7 CTAs of 128 threads). It loads the
-// weights while they fly, waits for its own copies only, then runs the FP32 fma chain
-// in k order from shared memory (slot [k][thread]: conflict-free) and stores 16 bytes.
+// GB300 design: a pure HBM stream (T*K rows of H BF16 in, T rows out). The unit of
+// work is one 16-byte fragment (8 columns) of one token, numbered flat over (token,
+// fragment) so that a warp covers 512 contiguous bytes of each row. The grid is
+// persistent (as many CTAs as fit: three per SM at K = 16) and thread i of the grid
+// takes the fragments i, i + G, i + 2G, ... (G threads in the grid). Each thread runs
+// its own ring of kStages shared-memory stages: it issues the asynchronous 16-byte
+// copies (cp.async, bypassing L1, evict-first in L2) of all K row fragments of the
+// next fragment, and loads that fragment's K weights into registers, before it waits
+// for and sums the current one. HBM thus always has the next items in flight and the
+// stream does not drain between waves of CTAs; the weights, loaded one item ahead,
+// never add their latency to an item. Slots are private to their thread ([stage][k]
+// [thread]: conflict-free), so no CTA barrier is needed. Per fragment: wait for its
+// copy group, FP32 fma chain in k order, one 16-byte store. Two stages and three CTAs
+// per SM keep more bytes in flight than three stages and two CTAs (the shared memory
+// of an SM holds six items either way).
 #include "common.cuh"
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -40,103 +47,145 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+
+constexpr int kStages = 2;
 
 // KT: compile-time K (0 = runtime K, up to MOE_MAX_TOPK).
 template <int KT, bool GATHER, bool BF16W, bool SHARED>
 __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
-  extern __shared__ __align__(16) uint4 slots[];  // [K][kThreads]
+  extern __shared__ __align__(16) uint4 slots[];  // [kStages][K (+1 shared)][kThreads]
   constexpr int KM = KT ? KT : MOE_MAX_TOPK;
   const int K = KT ? KT : a.K;
   const int frags = a.H >> 3;
-  const long long f = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const long long total = (long long)a.T * frags;
+  const long long stride = (long long)gridDim.x * kThreads;
+  const long long f0 = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const size_t H = (size_t)a.H;
   grid_launch_dependents();
   grid_wait();  // rows, weights and indices may come from the preceding kernel
-  if (f >= (long long)a.T * frags) return;
-  const int t = (int)(f / frags);
-  const int col = (int)(f - (long long)t * frags) * 8;
-  const size_t H = (size_t)a.H;
   const uint64_t pol = policy_evict_first();
   const uint32_t base = smem_u32(slots) + threadIdx.x * 16u;
+  const int SL = K + (SHARED ? 1 : 0);  // slots per stage: K rows, then the shared row
+  const uint32_t stage_bytes = (uint32_t)SL * kThreads * 16u;
 
-  // 1) every row copy in flight
-  bool use[KM];
+  // Copies of fragment fi's K row fragments (and its shared-row fragment) into stage
+  // st, as one commit group (empty past the end), and its K raw weights into wraw[st];
+  // returns the mask of rows not skipped.
+  using WRaw = typename std::conditional<BF16W, uint16_t, float>::type;
+  WRaw wraw[kStages][KM];
+  auto issue = [&](int st, long long fi) -> uint32_t {
+    uint32_t m = 0;
+    if (fi < total) {
+      const int t = (int)(fi / frags);
+      const int col = (int)(fi - (long long)t * frags) * 8;
 #pragma unroll
-  for (int k = 0; k < KM; ++k) {
-    use[k] = false;
-    if (KT || k < K) {
-      const size_t ix = (size_t)t * K + k;
-      long long r = GATHER ? (long long)__ldg(a.row_index + ix) : (long long)ix;
-      if (GATHER && (r < -1 || r >= a.n_rows)) {
-        set_error(a.err, MOE_DEVERR_ROW_INDEX);
-        r = -1;
+      for (int k = 0; k < KM; ++k) {
+        if (KT || k < K) {
+          const size_t ix = (size_t)t * K + k;
+          long long r = GATHER ? (long long)__ldg(a.row_index + ix) : (long long)ix;
+          if (GATHER && (r < -1 || r >= a.n_rows)) {
+            set_error(a.err, MOE_DEVERR_ROW_INDEX);
+            r = -1;
+          }
+          wraw[st][k] = __ldg(static_cast<const WRaw*>(a.weights) + ix);
+          if (r != -1) {
+            m |= 1u << k;
+            cp_async16(base + (uint32_t)st * stage_bytes + (uint32_t)(k * kThreads * 16), a.rows + (size_t)r * H + col,
+                       pol);
+          }
+        }
       }
-      use[k] = r != -1;
-      if (use[k]) cp_async16(base + (uint32_t)(k * kThreads * 16), a.rows + (size_t)r * H + col, pol);
+      if (SHARED)
+        cp_async16(base + (uint32_t)st * stage_bytes + (uint32_t)(K * kThreads * 16), a.shared + (size_t)t * H + col, pol);
+    }
+    cp_async_commit();
+    return m;
+  };
+
+  uint32_t mask[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) mask[s] = issue(s, f0 + s * stride);
+  for (long long f = f0; f < total; f += kStages * stride) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      const long long fi = f + s * stride;
+      constexpr int kAhead = kStages - 1;
+      const int sn = (s + kAhead) % kStages;
+      mask[sn] = issue(sn, fi + kAhead * stride);
+      if (fi >= total) break;
+      const int t = (int)(fi / frags);
+      const int col = (int)(fi - (long long)t * frags) * 8;
+      // the weights, loaded at issue, times routed_scaling_factor
+      float w[KM];
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        float wk = 0.0f;
+        if (KT || k < K) {
+          if constexpr (BF16W) wk = bf16_to_f32(wraw[s][k]); else wk = wraw[s][k];
+          if (a.scale != 1.0f) wk = __fmul_rn(wk, a.scale);
+        }
+        w[k] = wk;
+      }
+      cp_async_wait<kAhead>();
+      // FP32 fma over k in order
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      const uint4* sl = slots + (size_t)s * SL * kThreads + threadIdx.x;
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        if (!((mask[s] >> k) & 1u)) continue;
+        const uint4 v = sl[k * kThreads];
+        const uint32_t q4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = __fmaf_rn(w[k], bf16_lo(q4[q]), acc[2 * q]);
+          acc[2 * q + 1] = __fmaf_rn(w[k], bf16_hi(q4[q]), acc[2 * q + 1]);
+        }
+      }
+      if (SHARED) {
+        const uint4 sh = sl[K * kThreads];
+        const uint32_t q4[4] = {sh.x, sh.y, sh.z, sh.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(q4[q]));
+          acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(q4[q]));
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      st16(a.out + (size_t)t * H + col, o);
     }
   }
-  uint4 sh = make_uint4(0, 0, 0, 0);
-  if (SHARED) sh = ld_stream16(a.shared + (size_t)t * H + col, pol);
-  // 2) the weights while the rows fly
-  float w[KM];
-#pragma unroll
-  for (int k = 0; k < KM; ++k) {
-    float wk = 0.0f;
-    if (KT || k < K) {
-      const size_t ix = (size_t)t * K + k;
-      wk = BF16W ? bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.weights) + ix))
-                 : __ldg(static_cast<const float*>(a.weights) + ix);
-      if (a.scale != 1.0f) wk = __fmul_rn(wk, a.scale);
-    }
-    w[k] = wk;
-  }
-  cp_async_wait_all();
-  // 3) FP32 fma over k in order
-  float acc[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-#pragma unroll
-  for (int k = 0; k < KM; ++k) {
-    if (!use[k]) continue;
-    const uint4 v = slots[k * kThreads + threadIdx.x];
-    const uint32_t q4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[2 * q] = __fmaf_rn(w[k], bf16_lo(q4[q]), acc[2 * q]);
-      acc[2 * q + 1] = __fmaf_rn(w[k], bf16_hi(q4[q]), acc[2 * q + 1]);
-    }
-  }
-  if (SHARED) {
-    const uint32_t q4[4] = {sh.x, sh.y, sh.z, sh.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(q4[q]));
-      acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(q4[q]));
-    }
-  }
-  uint4 o;
-  o.x = pack_bf16x2(acc[0], acc[1]);
-  o.y = pack_bf16x2(acc[2], acc[3]);
-  o.z = pack_bf16x2(acc[4], acc[5]);
-  o.w = pack_bf16x2(acc[6], acc[7]);
-  st16(a.out + (size_t)t * H + col, o);
+  cp_async_wait<0>();
 }
 
 template <int KT, bool G, bool B, bool S>
-int launch_one(const FinArgs& a, cudaStream_t s) {
-  const size_t smem = (size_t)(KT ? KT : a.K) * kThreads * 16;
+int launch_one(const FinArgs& a, int sm_count, cudaStream_t s) {
+  const size_t smem = (size_t)kStages * ((KT ? KT : a.K) + (S ? 1 : 0)) * kThreads * 16;
   auto kern = finalize_kernel<KT, G, B, S>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
+    return MOE_ERR_CUDA;
   const long long threads = (long long)a.T * (a.H / 8);
-  return launch_pdl(kern, dim3((unsigned)((threads + kThreads - 1) / kThreads)), dim3(kThreads), smem, s, a);
+  const long long need = (threads + kThreads - 1) / kThreads;
+  const long long grid = need < (long long)sm_count * per_sm ? need : (long long)sm_count * per_sm;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, a);
 }
 
 template <int KT>
-int launch_variant(const FinArgs& a, bool gather, bool bf16w, bool shared, cudaStream_t s) {
+int launch_variant(const FinArgs& a, bool gather, bool bf16w, bool shared, int sm_count, cudaStream_t s) {
 #define MOE_FIN_CASE(G, B, S) \
-  if (gather == G && bf16w == B && shared == S) return launch_one<KT, G, B, S>(a, s);
+  if (gather == G && bf16w == B && shared == S) return launch_one<KT, G, B, S>(a, sm_count, s);
   MOE_FIN_CASE(false, false, false)
   MOE_FIN_CASE(false, false, true)
   MOE_FIN_CASE(false, true, false)
@@ -174,7 +223,7 @@ extern "C" int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t*
   FinArgs a{rows, (long long)n_rows, row_index, weights, shared, routed_scaling_factor, T, K, H, out, dev.error_word};
   const bool gather = row_index != nullptr, bf16w = weights_dtype == MOE_DTYPE_BF16, sh = shared != nullptr;
   cudaStream_t s = as_cuda(stream);
-  if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, s);
-  if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, s);
-  return launch_variant<0>(a, gather, bf16w, sh, s);
+  if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, dev.sm_count, s);
+  if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, dev.sm_count, s);
+  return launch_variant<0>(a, gather, bf16w, sh, dev.sm_count, s);
 }

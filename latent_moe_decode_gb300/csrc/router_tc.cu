@@ -296,6 +296,7 @@ int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, int T, int H, in
   auto kern = router_tc_kernel<BN, CLUSTER>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (prefer_max_shared(reinterpret_cast<const void*>(kern)) != MOE_OK) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, (T + BN - 1) / BN, (E + kBM - 1) / kBM);
   cfg.blockDim = dim3(kThreads);

@@ -1,5 +1,7 @@
 // Status strings, the device error word, and cached per-device facts.
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 
@@ -43,6 +45,26 @@ int current_device(DeviceInfo* out) {
     g_ready[dev] = true;
   }
   *out = g_info[dev];
+  return MOE_OK;
+}
+
+int prefer_max_shared(const void* func) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  static std::mutex mu;
+  static std::vector<std::pair<int, const void*>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == dev && d.second == func) return MOE_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  done.emplace_back(dev, func);
   return MOE_OK;
 }
 

@@ -34,6 +34,18 @@ def test_parity(moe, orc, T, K, E, skew):
     np.testing.assert_array_equal(host(pairs), epairs)
 
 
+@pytest.mark.parametrize("T,K,E,hi", [(100, 16, 896, 1), (300, 16, 896, 4), (2000, 16, 64, 40), (700, 8, 33, 33)])
+def test_parity_repeated_ids(moe, orc, T, K, E, hi):
+    """Ids drawn with repeats from [0, hi): whole warps of equal ids, which the
+    placement ranks as one group (the pages do not forbid repeats within a token)."""
+    ids = np.random.default_rng(T + hi).integers(0, hi, size=(T, K)).astype(np.int32)
+    off, pairs = moe.build_routing_lists(dev(ids), E)
+    torch.cuda.synchronize()
+    eoff, epairs = orc.routing_lists(ids, E)
+    np.testing.assert_array_equal(host(off), eoff)
+    np.testing.assert_array_equal(host(pairs), epairs)
+
+
 def test_bad_id_sets_error(moe):
     moe.device_error(clear=True)
     ids = np.array([[0, 1], [2, 9], [-1, 3]], np.int32)
