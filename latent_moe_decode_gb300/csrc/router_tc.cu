@@ -101,11 +101,36 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Store to the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, float v) {
+// The address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_dsmem(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+  return remote;
+}
+
+// Bulk copy (TMA engine) of `bytes` from this CTA's shared memory into another CTA's
+// shared memory of the cluster, completing `bytes` on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_remote, uint32_t src, uint32_t bytes, uint32_t bar_remote) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_remote),
+      "r"(src), "r"(bytes), "r"(bar_remote)
+      : "memory");
+}
+
+// Split-K reduction through the cluster: the BN token columns are cut into 16-column
+// chunks and CTA r of the S splits owns chunks [first(r), first(r + 1)). A chunk is
+// [16 columns][128 rows] FP32 (8 KB). The pipeline buffers, idle after the mainloop,
+// hold two staging chunks per warpgroup (64 KB) and S - 1 receive slices of up to
+// max_chunks(BN, S) chunks.
+constexpr uint32_t kStagingBytes = 4 * 2 * 8192;
+__host__ __device__ constexpr int chunk_first(int r, int nch, int S) { return (r * nch) / S; }
+__host__ __device__ constexpr int max_chunks(int bn, int S) { return (bn / 16 + S - 1) / S; }
+__host__ __device__ constexpr size_t reduce_bytes(int bn, int S) {
+  return kStagingBytes + (size_t)(S - 1) * max_chunks(bn, S) * 8192;
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // CLUSTER: the S split CTAs of a tile form one cluster and reduce through DSMEM.
@@ -126,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty = [&](int i) { return bar0 + 8u * (C::kStages + i); };
   const uint32_t accum = bar0 + 8u * (2 * C::kStages);
   const uint32_t slot = accum + 8u;
+  const uint32_t recvbar = accum + 16u;  // the other splits' partial slices have landed (cluster path)
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (slot - smem_u32(smem_raw)));
 
   if (threadIdx.x == 0) {
@@ -134,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty(i), 1);
     }
     mbar_init(accum, 1);
+    mbar_init(recvbar, 1);
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
@@ -194,51 +221,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's 32 TMEM lanes
   const int row = (warp & 3) * 32 + lane;                           // = expert row within the tile
   if constexpr (CLUSTER) {
-    // Every CTA of the cluster owns a slice of the tile's token columns. Once all
-    // mainloops are over (the pipeline buffers are idle everywhere), each CTA pushes
-    // each column of its partial straight into the owner's receive buffer
-    // recv[split][column - first][row] with remote shared-memory stores; after a
-    // second barrier every owner sums its slice over the splits in split order.
-    const int slice = (BN + S - 1) / S;
-    const uint32_t recv = base;  // the pipeline buffers: >= S * slice * 128 * 4 bytes
-    // column -> (owner CTA, byte offset of this split's slot in the owner's buffer),
-    // with owner r holding columns [(r * BN) / S, ((r + 1) * BN) / S)
-    __shared__ uint32_t s_dst[BN];
-    __shared__ uint32_t s_owner[BN];
-    for (int c = threadIdx.x; c < BN; c += kThreads) {
-      const int r = ((c + 1) * S - 1) / BN;
-      s_owner[c] = (uint32_t)r;
-      s_dst[c] = recv + (uint32_t)((s * slice + (c - (r * BN) / S)) * kBM * 4);
-    }
-    cluster_sync();  // also orders the tables above
-    if (done) {
+    // Split s owns the chunks [first(s), first(s + 1)) of the tile's columns. Every chunk
+    // of its partial that another split r owns goes to r: a warpgroup reads it from
+    // TMEM, stages it in one of its two staging chunks ([column][row]: 32 consecutive
+    // rows per store, conflict-free) and its first thread bulk-copies it (TMA engine)
+    // into r's receive slot for split s, completing the bytes on r's receive mbarrier.
+    // The four warpgroups take the chunks in turn and synchronise only among
+    // themselves. Then each owner waits for its S - 1 incoming slices and sums, per
+    // column, the S partials in split order -- its own read from TMEM -- and writes the
+    // logits. The partials never leave the chip.
+    constexpr int nch = BN / 16;
+    const int mc = max_chunks(BN, S);
+    const uint32_t slice = (uint32_t)mc * 8192u;
+    const uint32_t recv0 = base + kStagingBytes;
+    auto recv_slot = [&](int q, int owner) { return recv0 + (uint32_t)(q < owner ? q : q - 1) * slice; };
+    const int my0 = chunk_first(s, nch, S), my1 = chunk_first(s + 1, nch, S);
+    const bool lead = (threadIdx.x & 127) == 0;  // first thread of the warpgroup
+    if (threadIdx.x == 0)  // expect the other splits' bytes before any may arrive
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(recvbar),
+                   "r"((uint32_t)((S - 1) * (my1 - my0)) * 8192u)
+                   : "memory");
+    cluster_sync();  // every CTA is past its mainloop (its buffers are idle) and armed
+    int item = 0, issued = 0;
 #pragma unroll 1
-      for (int c0 = 16 * wg; c0 < BN; c0 += 16 * kGroups) {
-        uint32_t v[16];
-        tmem_ld16(tl + (uint32_t)c0, v);
-        tmem_wait_ld();
+    for (int k = 1; k < S; ++k) {
+      const int r = (s + k) % S;  // spread the copies over the owners
+      const int c0 = chunk_first(r, nch, S), c1 = chunk_first(r + 1, nch, S);
+#pragma unroll 1
+      for (int ch = c0; ch < c1; ++ch, ++item) {
+        if (item % kGroups != wg) continue;
+        const uint32_t stage = base + (uint32_t)(wg * 2 + (issued & 1)) * 8192u;
+        if (issued >= 2 && lead) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        named_sync(1 + wg, 128);  // the staging chunk's previous copy has read it
+        if (done) {
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)(16 * ch), v);
+          tmem_wait_ld();
+          const uint32_t col0 = stage + (uint32_t)row * 4u;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          st_dsmem(s_dst[c0 + j] + (uint32_t)(row * 4), s_owner[c0 + j], __uint_as_float(v[j]));
+          for (int j = 0; j < 16; ++j) asm volatile("st.shared.b32 [%0], %1;" ::"r"(col0 + 512u * j), "r"(v[j]) : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_sync(1 + wg, 128);
+        if (lead) {
+          bulk_s2cluster(map_dsmem(recv_slot(s, r) + (uint32_t)(ch - c0) * 8192u, (uint32_t)r), stage, 8192u,
+                         map_dsmem(recvbar, (uint32_t)r));
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        ++issued;
       }
     }
-    cluster_sync();  // every partial column is in its owner's buffer
-    const float* buf = reinterpret_cast<const float*>(smem_raw + (recv - smem_u32(smem_raw)));
-    const int c_lo = (s * BN) / S, c_hi = ((s + 1) * BN) / S;
-    const int r128 = threadIdx.x & (kBM - 1);
-    const int e = mt * kBM + r128;
-    for (int c = c_lo + (threadIdx.x >> 7); c < c_hi; c += kGroups) {
-      const int jj = c - c_lo;
-      float p[8];
+    const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(recvbar, 0, err));  // warp-uniform for tcgen05.ld
+    const int e = mt * kBM + row;
+    if (done && got) {
+      const float* rbase = reinterpret_cast<const float*>(smem_raw + (base - smem_u32(smem_raw)));
+#pragma unroll 1
+      for (int ch = my0 + wg; ch < my1; ch += kGroups) {
+        uint32_t v[16];
+        tmem_ld16(tl + (uint32_t)(16 * ch), v);
+        tmem_wait_ld();
+        float acc[16];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) p[q] = q < S ? buf[(q * slice + jj) * kBM + r128] : 0.0f;  // all loads first
-      float acc = p[0];
+        for (int q = 0; q < 8; ++q) {  // split order; each split's 16 columns loaded at once
+          if (q >= S) break;
+          float p[16];
+          if (q == s) {
 #pragma unroll
-      for (int q = 1; q < 8; ++q)
-        if (q < S) acc = __fadd_rn(acc, p[q]);  // then the sum, in split order
-      const int t = nt * BN + c;
-      if (t < T && e < E) out[(size_t)t * E + e] = acc;
+            for (int j = 0; j < 16; ++j) p[j] = __uint_as_float(v[j]);
+          } else {
+            const float* src = rbase + (kStagingBytes + (size_t)(q < s ? q : q - 1) * slice) / 4 +
+                               (size_t)(ch - my0) * 16 * kBM + row;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) p[j] = src[j * kBM];
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = q == 0 ? p[j] : __fadd_rn(acc[j], p[j]);
+        }
+        if (e < E) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = nt * BN + 16 * ch + j;
+            if (t < T) out[(size_t)t * E + e] = acc[j];
+          }
+        }
+      }
     }
+    if (lead) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // our copies have read
   } else if (done) {
     const int e = mt * kBM + row;
     float* dst = out + (size_t)s * T * E;
@@ -345,6 +413,16 @@ int max_clusters(int S) {
   return n;
 }
 
+size_t pipeline_bytes(int bn) {
+  switch (bn) {
+    case 16: return (size_t)Cfg<16>::kStages * Cfg<16>::kStageBytes;
+    case 32: return (size_t)Cfg<32>::kStages * Cfg<32>::kStageBytes;
+    case 64: return (size_t)Cfg<64>::kStages * Cfg<64>::kStageBytes;
+    case 128: return (size_t)Cfg<128>::kStages * Cfg<128>::kStageBytes;
+    default: return (size_t)Cfg<256>::kStages * Cfg<256>::kStageBytes;
+  }
+}
+
 int max_clusters_bn(int bn, int S) {
   switch (bn) {
     case 16: return max_clusters<16>(S);
@@ -374,9 +452,10 @@ TcPlan tc_plan(int T, int H, int E, int sm_count) {
   p.S = s;
   p.cluster = false;
   if (s >= 2 && s <= 8) {
-    // the largest cluster of splits whose clusters are all resident at once
+    // the largest cluster of splits whose clusters are all resident at once (and whose
+    // staging chunks and receive slices fit in the pipeline buffers)
     for (int c = s; c >= 2; --c) {
-      if (max_clusters_bn(p.bn, c) >= tiles) {
+      if (reduce_bytes(p.bn, c) <= pipeline_bytes(p.bn) && max_clusters_bn(p.bn, c) >= tiles) {
         p.S = c;
         p.cluster = true;
         break;
