@@ -10,21 +10,22 @@
 // expert e
 //   offsets[e]             = #{ i : 0 <= ids[i] < e }
 //   pairs[offsets[e] + r]  = the r-th i (ascending) with ids[i] == e
-// i.e. an order-preserving filter of the flat id array. That array is small (T*K*4
-// bytes, L2-resident), so every CTA scans all of it and owns a range of 32 experts: no
-// cross-CTA scan, no workspace, no global atomics, and few CTAs (28 for 896 experts).
-// Each of the 32 warps of a CTA owns a contiguous chunk of the ids and walks it in
-// steps of 32: lane l reads id step*32 + l (every load a coalesced 128 bytes). All 16
-// steps of a chunk (T*K <= 16384) are loaded at once -- one L2 round trip, since round
-// trips, not arithmetic, set this kernel's time. Pass 1 counts, per (warp, owned
-// expert), the matches (shared-memory atomics: counts do not depend on order) and,
-// per lane, the ids below the CTA's first expert; the owned slot of each loaded id
-// (or "none") stays in registers, a byte an id. Warp j then scans expert j's counts
-// over the warps (shuffles) into each warp's start within the expert's list, and warp
-// 0 scans the experts' totals into their offsets. Pass 2 places a block of 16 steps
-// without a serial chain: the ranks inside every step come from ballots at once (no
-// step waits on another), a per-warp table turns the steps' group sizes into per-step starts, and every
-// match is then written in parallel -- lists in ascending index order.
+// i.e. an order-preserving filter of the flat id array (T*K*4 bytes, L2-resident).
+// One thread-block cluster of kCluster CTAs per range of 32 experts; CTA c of a cluster
+// owns the c-th chunk of the ids, and each of its 16 warps a contiguous part of that,
+// walked in steps of 32 (lane l reads id step*32 + l: every load a coalesced 128
+// bytes; all steps of a part in flight at once -- one L2 round trip, since round trips,
+// not arithmetic, set this kernel's time). Pass 1 counts, per (warp, owned expert), the
+// matches (shared-memory atomics: counts do not depend on order) and, per lane, the ids
+// below the range; the owned slot of each loaded id (or "none") stays in registers, a
+// byte an id. Warp j scans expert j's counts over the warps (shuffles) into each warp's
+// start within the CTA's share. The CTAs then exchange their per-expert totals and
+// below-counts through distributed shared memory (after a cluster barrier), so each
+// knows where its share of every list starts, and CTA 0 writes the range's offsets.
+// Pass 2 places a block of 16 steps without a serial chain: the ranks inside every step
+// come from __match_any_sync at once (no step waits on another), a per-warp table turns
+// the steps' group sizes into per-step starts, and every match is then written in
+// parallel -- lists in ascending index order. No workspace, no global atomics.
 #include "common.cuh"
 
 namespace moe {
