@@ -245,6 +245,32 @@ int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index,
                  float routed_scaling_factor, int T, int K, int H, uint16_t* out,
                  moe_stream_t stream);
 
+/* -------------------------------------------------------------------------------
+ * The whole routing-and-combine step in one call.
+ * Source: [wide] WideMoE.run (router logits -> route -> ... -> Finalize of the
+ * token's top-K expert rows, on one stream) and [ep] EpMoeLayer.__call__.
+ *
+ * Launches, on `stream`, in this order (programmatic dependent launch between them):
+ *   moe_router_logits(x, w, logits, T, H, E, workspace, ...)
+ *   moe_topk_route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights,
+ *                           weights_bf16, latent, T, L, q, scales)
+ *   moe_build_routing_lists(ids, T, K, E, offsets, pairs)
+ *   moe_finalize(rows, T*K, NULL, weights_bf16, MOE_DTYPE_BF16, NULL, 1, T, K, L, out)
+ * i.e. Finalize combines the expanded expert rows (row t*K + k = token t's k-th
+ * expert) with the BF16 routing weights, as the wide page's Finalize does. Arguments,
+ * layouts and requirements are those of the four calls (weights may be NULL;
+ * weights_bf16 may not). `workspace` holds moe_route_finalize_workspace(T, H, E, K)
+ * bytes (NULL when that is 0); it is clobbered. Returns the first non-OK status of the
+ * four calls (the later ones are then not launched). Allocates nothing, so the call
+ * can be captured in a CUDA graph.
+ * ------------------------------------------------------------------------------- */
+size_t moe_route_finalize_workspace(int T, int H, int E, int K);
+int moe_route_finalize(const uint16_t* x, const uint16_t* w, const float* bias, const uint16_t* latent,
+                       const uint16_t* rows, int T, int H, int L, int E, int K, int renormalize, float scale,
+                       float* logits, int32_t* ids, float* weights, uint16_t* weights_bf16, int32_t* offsets,
+                       int32_t* pairs, uint8_t* q, uint8_t* scales, uint16_t* out, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

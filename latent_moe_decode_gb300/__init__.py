@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "load", "router_logits", "router_logits_workspace", "topk_route",
     "build_routing_lists", "build_routing_lists_workspace", "mxfp8_quantize_rows",
-    "finalize", "device_error", "RouteFinalize",
+    "finalize", "route_finalize", "route_finalize_workspace", "device_error", "RouteFinalize",
     "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05",
     "DEVERR_ROW_INDEX", "DEVERR_EXPERT_ID", "DEVERR_TIMEOUT",
 ]
@@ -45,6 +45,8 @@ SIGNATURES = {
     "moe_build_routing_lists": (_I, [_P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_finalize": (_I, [_P, ctypes.c_int64, _P, _P, _I, _P, _F, _I, _I, _I, _P, _P]),
+    "moe_route_finalize_workspace": (_SZ, [_I, _I, _I, _I]),
+    "moe_route_finalize": (_I, [_P] * 5 + [_I] * 6 + [_F] + [_P] * 9 + [_P, _SZ, _P]),
 }
 
 _lib = None
@@ -226,6 +228,39 @@ def device_error(clear: bool = True) -> int:
     return int(v.value)
 
 
+def route_finalize_workspace(T: int, H: int, E: int, K: int) -> int:
+    return int(load().moe_route_finalize_workspace(T, H, E, K))
+
+
+def route_finalize(x, w, bias, latent, rows, K: int, renormalize: bool, scale: float, logits, ids, weights,
+                   weights_bf16, offsets, pairs, q, scales, out, workspace=None, stream=None):
+    """The whole step in one library call (all outputs preallocated): router logits ->
+    top-K + MXFP8 -> routing lists -> Finalize of rows [T*K, L] with the BF16 weights."""
+    T, H = x.shape
+    E = w.shape[0]
+    L = latent.shape[1]
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(w, torch.bfloat16, (E, H), "w")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    _need(latent, torch.bfloat16, (T, L), "latent")
+    _need(rows, torch.bfloat16, (T * K, L), "rows")
+    for t, dt, shape, name in ((logits, torch.float32, (T, E), "logits"), (ids, torch.int32, (T, K), "ids"),
+                               (weights_bf16, torch.bfloat16, (T, K), "weights_bf16"),
+                               (offsets, torch.int32, (E + 1,), "offsets"), (pairs, torch.int32, (T * K,), "pairs"),
+                               (q, torch.uint8, (T, L), "q"), (scales, torch.uint8, (T, L // 32), "scales"),
+                               (out, torch.bfloat16, (T, L), "out")):
+        _need(t, dt, shape, name)
+    if weights is not None:
+        _need(weights, torch.float32, (T, K), "weights")
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_route_finalize", load().moe_route_finalize(
+        _ptr(x), _ptr(w), _ptr(bias), _ptr(latent), _ptr(rows), T, H, L, E, K, int(bool(renormalize)), float(scale),
+        _ptr(logits), _ptr(ids), _ptr(weights), _ptr(weights_bf16), _ptr(offsets), _ptr(pairs), _ptr(q), _ptr(scales),
+        _ptr(out), _ptr(workspace), ws, _stream(stream)))
+    return out
+
+
 class RouteFinalize:
     """The whole routing-and-combine step, with its buffers preallocated:
     router logits -> sigmoid+bias top-K with the MXFP8 latent in the same launch ->
@@ -235,7 +270,8 @@ class RouteFinalize:
 
     ``run()`` launches the library's kernels (programmatic dependent launch between
     consecutive kernels of a stream) and allocates nothing, so it can be captured in a
-    CUDA graph.
+    CUDA graph. With the automatic router choice it is one library call
+    (``moe_route_finalize``); with a forced router family, the four calls.
     """
 
     def __init__(self, T: int, H: int, L: int, E: int, K: int, device="cuda", renormalize=True, scale=1.0,
@@ -255,6 +291,7 @@ class RouteFinalize:
         self.out = e((T, L), torch.bfloat16)
         self.router_ws = e((max(1, router_logits_workspace(T, H, E)),), torch.uint8)
         self.lists_ws = e((max(1, build_routing_lists_workspace(T, K, E)),), torch.uint8)
+        self.chain_ws = e((max(1, route_finalize_workspace(T, H, E, K)),), torch.uint8)
         self.launches = self._count_launches()
 
     def _count_launches(self) -> int:
@@ -264,6 +301,10 @@ class RouteFinalize:
 
     def run(self, x, w, bias, latent, rows, stream=None):
         main = stream if stream is not None else torch.cuda.current_stream()
+        if self.router_algo == ROUTER_AUTO:
+            return route_finalize(x, w, bias, latent, rows, self.K, self.renormalize, self.scale, self.logits, self.ids,
+                                  self.weights, self.weights_bf16, self.offsets, self.pairs, self.q, self.scales,
+                                  self.out, workspace=self.chain_ws, stream=main)
         router_logits(x, w, out=self.logits, workspace=self.router_ws, algo=self.router_algo, stream=main)
         topk_route_quantize(self.logits, bias, self.K, latent, self.renormalize, self.scale, ids=self.ids,
                             weights=self.weights, weights_bf16=self.weights_bf16, q=self.q, scales=self.scales,

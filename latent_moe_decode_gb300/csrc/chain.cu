@@ -1,0 +1,32 @@
+// The routing-and-combine step as one call: the four launches of the chain, in order,
+// on the caller's stream (each kernel waits for its predecessor with programmatic
+// dependent launch, so the launches overlap their prologues).
+//
+// Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideMoE.run
+// (router -> route -> Finalize on one stream) and ...moe.ep.layer, EpMoeLayer.__call__.
+#include "common.cuh"
+
+extern "C" size_t moe_route_finalize_workspace(int T, int H, int E, int K) {
+  return moe_router_logits_workspace(T, H, E) + moe_build_routing_lists_workspace(T, K, E);
+}
+
+extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const float* bias, const uint16_t* latent,
+                                  const uint16_t* rows, int T, int H, int L, int E, int K, int renormalize,
+                                  float scale, float* logits, int32_t* ids, float* weights, uint16_t* weights_bf16,
+                                  int32_t* offsets, int32_t* pairs, uint8_t* q, uint8_t* scales, uint16_t* out,
+                                  void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (T < 1 || K < 1 || !weights_bf16) return MOE_ERR_INVALID_ARGUMENT;
+  const size_t rws = moe_router_logits_workspace(T, H, E);
+  const size_t lws = moe_build_routing_lists_workspace(T, K, E);
+  if (workspace_bytes < rws + lws || (rws + lws > 0 && !workspace)) return MOE_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int st = moe_router_logits(x, w, logits, T, H, E, ws, rws, stream);
+  if (st != MOE_OK) return st;
+  st = moe_topk_route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q,
+                               scales, stream);
+  if (st != MOE_OK) return st;
+  st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws : nullptr, lws, stream);
+  if (st != MOE_OK) return st;
+  return moe_finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out,
+                      stream);
+}

@@ -78,6 +78,12 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.moe_router_logits_ex(A16, A16, A16, 0, 7168, 896, None, 0, 0, None) == 1
     assert lib.moe_router_logits_ex(A16, A16, A16, 8, 7167, 896, None, 0, 0, None) == 1
     assert lib.moe_router_logits_ex(A16, A16, A16, 8, 7168, 896, None, 0, 7, None) == 1
+    # the whole step: T >= 1, K >= 1, BF16 weights required
+    chain = lambda T, K, wb: lib.moe_route_finalize(A16, A16, None, A16, A16, T, 7168, 3584, 896, K, 1, 1.0, A16, A16,
+                                                    None, wb, A16, A16, A16, A16, A16, None, 0, None)
+    assert chain(0, 16, A16) == 1
+    assert chain(8, 0, A16) == 1
+    assert chain(8, 16, None) == 1
     assert lib.moe_router_logits_ex(P(264), A16, A16, 8, 7168, 896, None, 0, 0, None) == 2
 
 

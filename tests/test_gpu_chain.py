@@ -77,3 +77,21 @@ def test_skew_sweep(moe, orc, T):
 
 def test_wide_in_cuda_graph(moe, orc):
     _check_chain(moe, orc, 1020, samples=2000, graph=True)
+
+
+@pytest.mark.parametrize("T", [8, 1020])
+def test_one_call_equals_four_calls(moe, T):
+    """moe_route_finalize == the four calls it stands for, every output bit for bit."""
+    d = synth.chain_inputs(T, seed=3)
+    x, w, bias, latent, rows = bf16_dev(d["x"]), bf16_dev(d["w"]), dev(d["bias"]), bf16_dev(d["latent"]), bf16_dev(d["rows"])
+    one = moe.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K)
+    one.run(x, w, bias, latent, rows)
+    logits = moe.router_logits(x, w)
+    ids, wf, wb, q, sc = moe.topk_route_quantize(logits, bias, synth.K, latent)
+    off, pairs = moe.build_routing_lists(ids, synth.E)
+    out = moe.finalize(rows, wb, T, synth.K)
+    torch.cuda.synchronize()
+    for name, b in (("logits", logits), ("ids", ids), ("weights", wf), ("weights_bf16", wb), ("offsets", off),
+                    ("pairs", pairs), ("q", q), ("scales", sc), ("out", out)):
+        a = getattr(one, name)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name
