@@ -22,8 +22,10 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int st = moe_router_logits(x, w, logits, T, H, E, ws, rws, stream);
   if (st != MOE_OK) return st;
-  st = moe_topk_route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q,
-                               scales, stream);
+  // the latent is an input of the step, complete before the router started: the
+  // quantisation CTAs run beside the router instead of after it
+  st = moe::route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q,
+                           scales, true, moe::as_cuda(stream));
   if (st != MOE_OK) return st;
   st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws : nullptr, lws, stream);
   if (st != MOE_OK) return st;

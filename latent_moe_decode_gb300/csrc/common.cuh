@@ -26,6 +26,14 @@ int current_device(DeviceInfo* out);
 // beside, or (programmatic dependent launch) right behind, the previous one.
 int prefer_max_shared(const void* func);
 
+// Sigmoid top-K and MXFP8 of the latent in one launch (moe_topk_route_quantize). With
+// latent_ready the quantisation CTAs do not wait for the preceding kernel: only for a
+// latent complete before that kernel started, and a preceding kernel that signals its
+// dependents after its own wait (the router kernels do).
+int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
+                   int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
+                   uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s);
+
 inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

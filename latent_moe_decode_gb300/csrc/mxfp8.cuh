@@ -15,10 +15,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-// One CTA's 16-byte chunks [block * THREADS * UNROLL, ...) of the flat input.
+// One CTA's 16-byte chunks [block * THREADS * UNROLL, ...) of the flat input. With
+// wait = false the CTA does not wait for the preceding kernel (the caller knows the
+// input was complete before that kernel started).
 template <int THREADS, int UNROLL>
 __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long long nchunks, uint8_t* __restrict__ q,
-                                            uint8_t* __restrict__ scales, uint32_t* err, long long block) {
+                                            uint8_t* __restrict__ scales, uint32_t* err, long long block,
+                                            bool wait = true) {
   constexpr int kThreads = THREADS, kUnroll = UNROLL;
   __shared__ __align__(128) uint4 stage[kThreads * kUnroll];
   __shared__ __align__(8) uint64_t bar_mem;
@@ -32,7 +35,7 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
   }
   __syncthreads();  // the barrier is initialised before any thread waits on it
   grid_launch_dependents();
-  grid_wait();
+  if (wait) grid_wait();
   if (threadIdx.x == 0) {
     mbar_expect_tx(bar, (uint32_t)nch * 16u);
     bulk_g2s(smem_u32(stage), x + cta0 * 8, (uint32_t)nch * 16u, bar, policy_evict_first());

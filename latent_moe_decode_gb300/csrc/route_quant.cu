@@ -6,9 +6,12 @@
 //
 // GB300 design: the two jobs share nothing, so in one grid the quantisation CTAs
 // stream the latent through HBM on the SMs the routing CTAs leave free, instead of
-// running after them. CTAs [0, T) run the top-K selection of token t (topk.cuh);
-// CTAs [T, T + Q) each quantise a 16 KB span of the latent (mxfp8.cuh), one bulk copy
-// per CTA. Both bodies are the ones the separate calls use, so the results are
+// running after them. T CTAs run the top-K selection of one token each (topk.cuh) and
+// Q CTAs each quantise a 16 KB span of the latent (mxfp8.cuh), one bulk copy per CTA.
+// Inside moe_route_finalize the latent is an input of the whole step, so the
+// quantisation CTAs need not wait for the router (the router signals its dependents
+// only after its own wait): they come first in the grid and run on the SMs the router
+// leaves idle. Both bodies are the ones the separate calls use, so the results are
 // identical to moe_topk_route followed by mxfp8_quantize_rows.
 #include "mxfp8.cuh"
 #include "topk.cuh"
@@ -22,21 +25,29 @@ constexpr int kQuantUnroll = 8;  // 128 threads x 8 chunks = 16 KB per quantisat
 template <int NJ>
 __global__ void __launch_bounds__(kThreads) route_quant_kernel(const TopkArgs a, const uint16_t* __restrict__ x,
                                                                long long nchunks, uint8_t* __restrict__ q,
-                                                               uint8_t* __restrict__ scales, uint32_t* err) {
-  if ((int)blockIdx.x < a.T)
-    topk_token<NJ>(a, (int)blockIdx.x);
-  else
-    mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)blockIdx.x - a.T);
+                                                               uint8_t* __restrict__ scales, uint32_t* err, int qblocks,
+                                                               int quant_wait) {
+  // Blocks are dispatched in index order. When the quantisation CTAs need not wait they
+  // come first and take the SMs that are free while the preceding kernel still runs;
+  // otherwise the routing CTAs (the longer ones) come first.
+  const int b = (int)blockIdx.x;
+  if (quant_wait) {
+    if (b < a.T) topk_token<NJ>(a, b);
+    else mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)(b - a.T), true);
+  } else {
+    if (b < qblocks) mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)b, false);
+    else topk_token<NJ>(a, b - qblocks);
+  }
 }
 
 }  // namespace
 }  // namespace moe
 
-extern "C" int moe_topk_route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize,
-                                       float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,
-                                       const uint16_t* latent, int rows, int cols, uint8_t* q, uint8_t* scales,
-                                       moe_stream_t stream) {
-  using namespace moe;
+namespace moe {
+
+int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
+                   int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
+                   uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s) {
   using namespace moe::topk_impl;
   if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARGUMENT;
   if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK) return MOE_ERR_CAPACITY;
@@ -55,11 +66,11 @@ extern "C" int moe_topk_route_quantize(const float* logits, const float* bias, i
   if (st != MOE_OK) return st;
   TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
   const dim3 grid((unsigned)(T + qblocks)), block(kThreads);
-  cudaStream_t s = as_cuda(stream);
+  const int qb = (int)qblocks, qw = latent_ready ? 0 : 1;
   switch ((E + 127) / 128) {
 #define MOE_RQ_CASE(N) \
   case N:              \
-    return launch_pdl(route_quant_kernel<N>, grid, block, 0, s, a, latent, nchunks, q, scales, dev.error_word);
+    return launch_pdl(route_quant_kernel<N>, grid, block, 0, s, a, latent, nchunks, q, scales, dev.error_word, qb, qw);
     MOE_RQ_CASE(1)
     MOE_RQ_CASE(2)
     MOE_RQ_CASE(3)
@@ -71,4 +82,14 @@ extern "C" int moe_topk_route_quantize(const float* logits, const float* bias, i
 #undef MOE_RQ_CASE
   }
   return MOE_ERR_CAPACITY;
+}
+
+}  // namespace moe
+
+extern "C" int moe_topk_route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize,
+                                       float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,
+                                       const uint16_t* latent, int rows, int cols, uint8_t* q, uint8_t* scales,
+                                       moe_stream_t stream) {
+  return moe::route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, rows, cols,
+                             q, scales, false, moe::as_cuda(stream));
 }

@@ -32,8 +32,8 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
   const int kb = s * kc;
   const int len8 = (min(H, kb + kc) - kb) / 8;
   const int row8 = kc / 8;
-  grid_launch_dependents();
   grid_wait();
+  grid_launch_dependents();  // after the wait: dependents may rely on all before the router
   for (int i = threadIdx.x; i < 16 * len8; i += kThreads) {
     const int tt = i / len8, kk = i - tt * len8;
     xs[tt * row8 + kk] = (t0 + tt < T) ? ld_nc16(x + (size_t)(t0 + tt) * H + kb + kk * 8) : make_uint4(0, 0, 0, 0);
@@ -78,8 +78,8 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
 
 __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ part, int S, long long n,
                                                             float* __restrict__ logits) {
-  grid_launch_dependents();
   grid_wait();
+  grid_launch_dependents();  // after the wait: dependents may rely on all before the router
   for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
     float v = part[i];
     for (int s = 1; s < S; ++s) v = __fadd_rn(v, part[(size_t)s * n + i]);

@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *slot_ptr;
 
-  grid_launch_dependents();
-  grid_wait();  // x (and the gate) may be written by the preceding kernel
+  grid_wait();
+  grid_launch_dependents();  // after the wait: dependents may rely on all before the router  // x (and the gate) may be written by the preceding kernel
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
