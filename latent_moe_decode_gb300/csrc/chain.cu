@@ -29,6 +29,9 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   if (st != MOE_OK) return st;
   st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws : nullptr, lws, stream);
   if (st != MOE_OK) return st;
-  return moe_finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out,
-                      stream);
+  // Finalize reads only the step's rows and top-K's weights, both complete once the lists
+  // kernel has passed its own wait (it signals its dependents only then): Finalize runs
+  // beside the lists instead of after them.
+  return moe::finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out, true,
+                       moe::as_cuda(stream));
 }

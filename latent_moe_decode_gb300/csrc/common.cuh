@@ -34,6 +34,13 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
                    uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s);
 
+// Finalize (moe_finalize). With inputs_ready the kernel does not wait for the preceding
+// kernel: only when rows, weights and indices were complete before that kernel was
+// launched (it runs beside it).
+int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, const void* weights, int weights_dtype,
+             const uint16_t* shared, float routed_scaling_factor, int T, int K, int H, uint16_t* out,
+             bool inputs_ready, cudaStream_t s);
+
 inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

@@ -41,6 +41,7 @@ struct FinArgs {
   int T, K, H;
   uint16_t* out;
   uint32_t* err;
+  int wait;  // wait for the preceding kernel before reading (0: the caller knows the inputs are ready)
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   const long long f0 = (long long)blockIdx.x * kThreads + threadIdx.x;
   const size_t H = (size_t)a.H;
   grid_launch_dependents();
-  grid_wait();  // rows, weights and indices may come from the preceding kernel
+  if (a.wait) grid_wait();  // rows, weights and indices may come from the preceding kernel
   const uint64_t pol = policy_evict_first();
   const uint32_t base = smem_u32(slots) + threadIdx.x * 16u;
   const int SL = K + (SHARED ? 1 : 0);  // slots per stage: K rows, then the shared row
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     }
   }
   cp_async_wait<0>();
+  if (!a.wait) grid_wait();  // not done before the preceding kernel: stream order holds for what follows
 }
 
 template <int KT, bool G, bool B, bool S>
@@ -201,11 +203,11 @@ int launch_variant(const FinArgs& a, bool gather, bool bf16w, bool shared, int s
 }  // namespace
 }  // namespace moe
 
-extern "C" int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index,
-                            const void* weights, int weights_dtype, const uint16_t* shared,
-                            float routed_scaling_factor, int T, int K, int H, uint16_t* out,
-                            moe_stream_t stream) {
-  using namespace moe;
+namespace moe {
+
+int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, const void* weights, int weights_dtype,
+             const uint16_t* shared, float routed_scaling_factor, int T, int K, int H, uint16_t* out,
+             bool inputs_ready, cudaStream_t s) {
   if (T < 0 || K < 1 || K > MOE_MAX_TOPK || H < 8 || H % 8 != 0 || n_rows < 0)
     return MOE_ERR_INVALID_ARGUMENT;
   if (weights_dtype != MOE_DTYPE_F32 && weights_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARGUMENT;
@@ -220,10 +222,20 @@ extern "C" int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t*
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
 
-  FinArgs a{rows, (long long)n_rows, row_index, weights, shared, routed_scaling_factor, T, K, H, out, dev.error_word};
+  FinArgs a{rows, (long long)n_rows, row_index, weights, shared, routed_scaling_factor, T, K, H, out, dev.error_word,
+            inputs_ready ? 0 : 1};
   const bool gather = row_index != nullptr, bf16w = weights_dtype == MOE_DTYPE_BF16, sh = shared != nullptr;
-  cudaStream_t s = as_cuda(stream);
   if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, dev.sm_count, s);
   if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, dev.sm_count, s);
   return launch_variant<0>(a, gather, bf16w, sh, dev.sm_count, s);
+}
+
+}  // namespace moe
+
+extern "C" int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index,
+                            const void* weights, int weights_dtype, const uint16_t* shared,
+                            float routed_scaling_factor, int T, int K, int H, uint16_t* out,
+                            moe_stream_t stream) {
+  return moe::finalize(rows, n_rows, row_index, weights, weights_dtype, shared, routed_scaling_factor, T, K, H, out,
+                       false, moe::as_cuda(stream));
 }

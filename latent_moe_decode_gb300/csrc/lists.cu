@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
   s_cnt[warp][lane] = 0;
   __syncthreads();
 
-  grid_launch_dependents();
   grid_wait();
+  grid_launch_dependents();  // after the wait: dependents may rely on all before the lists
 
   // pass 1
   int* cnt = s_cnt[warp];
