@@ -223,6 +223,24 @@ def time_region(fn, n, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def max_over_ranks(values, world, device):
+    """Each value's maximum over the ranks (the slowest rank's time); the identity on
+    one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(T, world, ms):
+    """Tokens per second of all ranks together: each rank runs its own T-token step
+    (the path shards by token, no exchange), timed by the slowest rank."""
+    return world * T / (ms * 1e-3)
+
+
 COLD_FACTOR = 3  # a rotation of input copies moves at least this many L2 capacities
 L2_BYTES = 129 << 20
 
@@ -353,10 +371,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
     if rank != 0:
         return None
 
@@ -373,7 +388,7 @@ def run_ours(args, rank, world, local_rank):
     steps["router"]["frac_bf16"] = round(flops / (per_ms["router"] * 1e-3) / 1e12 / bf16, 3)
     line = {
         "metric": METRIC,
-        "value": round(world * T / (ms * 1e-3), 1),
+        "value": round(whole_job_rate(T, world, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -397,7 +412,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(fin_gbs / hbm, 3), "traffic": traffic, "alg_bytes_per_launch": ab["finalize"],
                      "peak_source": f"{peak_src}: copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"},
         "steps_alone": steps,
-        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
+        "e2e": {"value": round(whole_job_rate(T, world, e2e_ms), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * rf.launches,
         "clocks": clocks,

@@ -1,0 +1,56 @@
+"""The bench's N-rank host logic on CPU with two gloo ranks (the path itself has no
+exchange: each rank runs its own replica; the ranks only agree on the slowest time)."""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.5 * rank], world, "cpu")
+        args = type("A", (), {"steps": 1, "warmup": 0, "cpu_seconds": 0.1})()
+        ref_line = bench.run_reference(args, rank) if rank != 0 else "rank0"
+        out.put((rank, got, ref_line))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = dict((r, (g, l)) for r, g, l in (out.get(timeout=120) for _ in procs))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert results[0][0] == results[1][0] == [2.0, 10.0, 0.5]
+    assert results[1][1] is None  # only rank 0 runs and prints the reference arm
+
+
+def test_whole_job_rate_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.whole_job_rate(1020, 1, 1.0) == pytest.approx(1.02e6)
+    assert bench.whole_job_rate(1020, 4, 1.0) == pytest.approx(4.08e6)
+    assert bench.max_over_ranks([3.0, 4.0], 1, "cpu") == [3.0, 4.0]
