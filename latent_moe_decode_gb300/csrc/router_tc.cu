@@ -449,6 +449,9 @@ TcPlan tc_plan(int T, int H, int E, int sm_count) {
   s = s < 1 ? 1 : s;
   s = s > 32 ? 32 : s;
   if (s > p.n_kb / 2) s = p.n_kb / 2 > 0 ? p.n_kb / 2 : 1;
+  // at most one portable cluster of splits: at small T the on-chip reduction in one
+  // kernel beats more splits reduced through a workspace by a second kernel
+  if (s > 8) s = 8;
   p.S = s;
   p.cluster = false;
   if (s >= 2 && s <= 8) {

@@ -70,8 +70,9 @@ def test_wide(moe, orc):
     _check_chain(moe, orc, 1020, samples=4000)
 
 
-@pytest.mark.parametrize("T", [1, 16, 256, 4096])
+@pytest.mark.parametrize("T", [1, 16, 64, 256, 1020, 4096])
 def test_skew_sweep(moe, orc, T):
+    """The skew sweep's token counts, Zipf(1.1) expert popularity."""
     _check_chain(moe, orc, T, skew=True, samples=None if T <= 16 else 3000)
 
 
