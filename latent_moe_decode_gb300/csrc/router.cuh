@@ -15,11 +15,15 @@ struct TcPlan {
   int bn;    // token tile: 16, 32, 64, 128 or 256
   int S;     // K splits
   int n_kb;  // 64-wide K blocks
-  bool cluster;  // splits reduced on chip through distributed shared memory (no workspace)
+  bool cluster;  // the S splits of a tile form a cluster and reduce in one kernel (partials through L2)
 };
-// Split-K workspace a plan needs (bytes).
+// Split-K workspace a plan needs (bytes): the partials [S][T][E] of the two-kernel
+// reduction, or, for a cluster plan, every tile's S partial tiles [BN][128].
 inline size_t tc_workspace(const TcPlan& p, int T, int E) {
-  return (p.S > 1 && !p.cluster) ? (size_t)p.S * T * E * sizeof(float) : 0;
+  if (p.S <= 1) return 0;
+  if (!p.cluster) return (size_t)p.S * T * E * sizeof(float);
+  const size_t tiles = (size_t)((E + 127) / 128) * ((T + p.bn - 1) / p.bn);
+  return tiles * p.S * p.bn * 128 * sizeof(float);
 }
 TcPlan tc_plan(int T, int H, int E, int sm_count);
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,

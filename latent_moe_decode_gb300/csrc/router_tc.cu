@@ -22,12 +22,16 @@
 //     instruction writes 128 contiguous bytes. The epilogue is latency-bound, hence the
 //     many warps although the mainloop needs two threads.
 // Split-K: when the S split CTAs of a tile fit as one thread-block cluster (S <= 8,
-// all co-resident), each parks its FP32 partial tile in its own shared memory (the
-// pipeline buffers are idle by then), and after a cluster barrier every CTA sums a
-// share of the tile's token columns over the S partials -- read through distributed
-// shared memory, in split order -- and writes final logits: the partials never leave
-// the chip. Otherwise (many splits at small batches) the partials [S][T][E] go to the
-// caller's workspace and a second kernel sums them in split order.
+// all co-resident), the reduction happens in the same kernel: the tile's token columns
+// are cut into 16-column chunks shared out among the S CTAs; after the mainloops each
+// CTA writes the chunks other splits own from TMEM to the caller's workspace (128
+// contiguous bytes per warp store, L2-resident), a cluster barrier orders those writes
+// before the reads, and each owner sums its chunks over the S partials in split order
+// (its own straight from TMEM), writes final logits (lanes = consecutive experts: 128
+// contiguous bytes per store) and invalidates the workspace lines it read in L2
+// (discard.global.L2), so the scratch never costs an HBM write-back. Otherwise (more
+// splits) the partials [S][T][E] go to the workspace and a second kernel sums them in
+// split order.
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel sets
 // MOE_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies in flight,
 // frees its TMEM and exits.
@@ -101,43 +105,15 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t map_dsmem(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  return remote;
-}
-
-// Bulk copy (TMA engine) of `bytes` from this CTA's shared memory into another CTA's
-// shared memory of the cluster, completing `bytes` on that CTA's mbarrier.
-__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_remote, uint32_t src, uint32_t bytes, uint32_t bar_remote) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_remote),
-      "r"(src), "r"(bytes), "r"(bar_remote)
-      : "memory");
-}
-
-// Split-K reduction through the cluster: the BN token columns are cut into 16-column
-// chunks and CTA r of the S splits owns chunks [first(r), first(r + 1)). A chunk is
-// [16 columns][128 rows] FP32 (8 KB). The pipeline buffers, idle after the mainloop,
-// hold two staging chunks per warpgroup (64 KB) and S - 1 receive slices of up to
-// max_chunks(BN, S) chunks.
-constexpr uint32_t kStagingBytes = 4 * 2 * 8192;
+// The BN token columns of a tile are cut into 16-column chunks; split r of S owns the
+// chunks [first(r), first(r + 1)).
 __host__ __device__ constexpr int chunk_first(int r, int nch, int S) { return (r * nch) / S; }
-__host__ __device__ constexpr int max_chunks(int bn, int S) { return (bn / 16 + S - 1) / S; }
-__host__ __device__ constexpr size_t reduce_bytes(int bn, int S) {
-  return kStagingBytes + (size_t)(S - 1) * max_chunks(bn, S) * 8192;
-}
-
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 // CLUSTER: the S split CTAs of a tile form one cluster and reduce through DSMEM.
 template <int BN, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, float* out,
-                     int T, int E, int n_kb, int S, uint32_t* err) {
+                     float* part, int T, int E, int n_kb, int S, int discard, uint32_t* err) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty = [&](int i) { return bar0 + 8u * (C::kStages + i); };
   const uint32_t accum = bar0 + 8u * (2 * C::kStages);
   const uint32_t slot = accum + 8u;
-  const uint32_t recvbar = accum + 16u;  // the other splits' partial slices have landed (cluster path)
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (slot - smem_u32(smem_raw)));
 
   if (threadIdx.x == 0) {
@@ -160,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty(i), 1);
     }
     mbar_init(accum, 1);
-    mbar_init(recvbar, 1);
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
@@ -221,60 +195,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's 32 TMEM lanes
   const int row = (warp & 3) * 32 + lane;                           // = expert row within the tile
   if constexpr (CLUSTER) {
-    // Split s owns the chunks [first(s), first(s + 1)) of the tile's columns. Every chunk
-    // of its partial that another split r owns goes to r: a warpgroup reads it from
-    // TMEM, stages it in one of its two staging chunks ([column][row]: 32 consecutive
-    // rows per store, conflict-free) and its first thread bulk-copies it (TMA engine)
-    // into r's receive slot for split s, completing the bytes on r's receive mbarrier.
-    // The four warpgroups take the chunks in turn and synchronise only among
-    // themselves. Then each owner waits for its S - 1 incoming slices and sums, per
-    // column, the S partials in split order -- its own read from TMEM -- and writes the
-    // logits. The partials never leave the chip.
+    // Split s owns the 16-column chunks [first(s), first(s + 1)) of the tile. It writes
+    // the chunks other splits own from TMEM to its slot of the workspace ([column][128
+    // rows] FP32: every store instruction of a warp writes 128 contiguous bytes; 18 MB
+    // at T = 1020, resident in L2). After a cluster barrier (release / acquire at cluster
+    // scope) each owner reads its chunks of the other S - 1 partials, all loads of a
+    // split at once, sums them per column in split order with its own partial (read
+    // from TMEM) and writes the logits; it then invalidates the workspace lines it read
+    // in L2 (discard.global.L2), so the scratch is never written back to HBM.
     constexpr int nch = BN / 16;
-    const int mc = max_chunks(BN, S);
-    const uint32_t slice = (uint32_t)mc * 8192u;
-    const uint32_t recv0 = base + kStagingBytes;
-    auto recv_slot = [&](int q, int owner) { return recv0 + (uint32_t)(q < owner ? q : q - 1) * slice; };
     const int my0 = chunk_first(s, nch, S), my1 = chunk_first(s + 1, nch, S);
-    const bool lead = (threadIdx.x & 127) == 0;  // first thread of the warpgroup
-    if (threadIdx.x == 0)  // expect the other splits' bytes before any may arrive
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(recvbar),
-                   "r"((uint32_t)((S - 1) * (my1 - my0)) * 8192u)
-                   : "memory");
-    cluster_sync();  // every CTA is past its mainloop (its buffers are idle) and armed
-    int item = 0, issued = 0;
+    const size_t tile = (size_t)mt * gridDim.y + nt;
+    float* slot = part + (tile * S + s) * (size_t)BN * kBM;
+    if (done) {
 #pragma unroll 1
-    for (int k = 1; k < S; ++k) {
-      const int r = (s + k) % S;  // spread the copies over the owners
-      const int c0 = chunk_first(r, nch, S), c1 = chunk_first(r + 1, nch, S);
-#pragma unroll 1
-      for (int ch = c0; ch < c1; ++ch, ++item) {
-        if (item % kGroups != wg) continue;
-        const uint32_t stage = base + (uint32_t)(wg * 2 + (issued & 1)) * 8192u;
-        if (issued >= 2 && lead) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        named_sync(1 + wg, 128);  // the staging chunk's previous copy has read it
-        if (done) {
-          uint32_t v[16];
-          tmem_ld16(tl + (uint32_t)(16 * ch), v);
-          tmem_wait_ld();
-          const uint32_t col0 = stage + (uint32_t)row * 4u;
+      for (int ch = wg; ch < nch; ch += kGroups) {
+        if (ch >= my0 && ch < my1) continue;
+        uint32_t v[16];
+        tmem_ld16(tl + (uint32_t)(16 * ch), v);
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) asm volatile("st.shared.b32 [%0], %1;" ::"r"(col0 + 512u * j), "r"(v[j]) : "memory");
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        named_sync(1 + wg, 128);
-        if (lead) {
-          bulk_s2cluster(map_dsmem(recv_slot(s, r) + (uint32_t)(ch - c0) * 8192u, (uint32_t)r), stage, 8192u,
-                         map_dsmem(recvbar, (uint32_t)r));
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        ++issued;
+        for (int j = 0; j < 16; ++j) __stcg(slot + (size_t)(16 * ch + j) * kBM + row, __uint_as_float(v[j]));
       }
     }
-    const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(recvbar, 0, err));  // warp-uniform for tcgen05.ld
+    cluster_sync();  // every split's partial chunks are written and visible to the cluster
     const int e = mt * kBM + row;
-    if (done && got) {
-      const float* rbase = reinterpret_cast<const float*>(smem_raw + (base - smem_u32(smem_raw)));
+    if (done) {
 #pragma unroll 1
       for (int ch = my0 + wg; ch < my1; ch += kGroups) {
         uint32_t v[16];
@@ -289,13 +235,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) p[j] = __uint_as_float(v[j]);
           } else {
-            const float* src = rbase + (kStagingBytes + (size_t)(q < s ? q : q - 1) * slice) / 4 +
-                               (size_t)(ch - my0) * 16 * kBM + row;
+            const float* src = part + ((tile * S + q) * (size_t)BN + 16 * ch) * kBM + row;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) p[j] = src[j * kBM];
+            for (int j = 0; j < 16; ++j) p[j] = __ldcg(src + (size_t)j * kBM);
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[j] = q == 0 ? p[j] : __fadd_rn(acc[j], p[j]);
+        }
+        __syncwarp();  // every lane's loads are consumed before their lines are invalidated
+        if (discard && lane < 16) {  // (a workspace aligned to 128 bytes: whole lines)
+          for (int q = 0; q < S; ++q) {
+            if (q == s) continue;
+            const float* line = part + ((tile * S + q) * (size_t)BN + 16 * ch + lane) * kBM + (warp & 3) * 32;
+            asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+          }
         }
         if (e < E) {
 #pragma unroll
@@ -306,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lead) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // our copies have read
   } else if (done) {
     const int e = mt * kBM + row;
     float* dst = out + (size_t)s * T * E;
@@ -357,8 +309,8 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows)
 }
 
 template <int BN, bool CLUSTER>
-int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, int T, int H, int E, const TcPlan& p, uint32_t* err,
-              cudaStream_t stream) {
+int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, float* part, int T, int H, int E, const TcPlan& p,
+              uint32_t* err, cudaStream_t stream) {
   CUtensorMap tm_w, tm_x;
   if (!make_map(&tm_w, w, E, H, kBM) || !make_map(&tm_x, x, T, H, BN)) return MOE_ERR_CUDA;
   auto kern = router_tc_kernel<BN, CLUSTER>;
@@ -379,7 +331,10 @@ int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, int T, int H, in
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CLUSTER ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, dst, T, E, p.n_kb, p.S, err) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const int discard = (reinterpret_cast<uintptr_t>(part) & 127u) == 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, dst, part, T, E, p.n_kb, p.S, discard, err) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 // Clusters of S split CTAs (one tile each) that can be resident at once.
@@ -411,16 +366,6 @@ int max_clusters(int S) {
   }
   cache[S] = n > 0 ? n : -1;
   return n;
-}
-
-size_t pipeline_bytes(int bn) {
-  switch (bn) {
-    case 16: return (size_t)Cfg<16>::kStages * Cfg<16>::kStageBytes;
-    case 32: return (size_t)Cfg<32>::kStages * Cfg<32>::kStageBytes;
-    case 64: return (size_t)Cfg<64>::kStages * Cfg<64>::kStageBytes;
-    case 128: return (size_t)Cfg<128>::kStages * Cfg<128>::kStageBytes;
-    default: return (size_t)Cfg<256>::kStages * Cfg<256>::kStageBytes;
-  }
 }
 
 int max_clusters_bn(int bn, int S) {
@@ -455,10 +400,9 @@ TcPlan tc_plan(int T, int H, int E, int sm_count) {
   p.S = s;
   p.cluster = false;
   if (s >= 2 && s <= 8) {
-    // the largest cluster of splits whose clusters are all resident at once (and whose
-    // staging chunks and receive slices fit in the pipeline buffers)
+    // the largest cluster of splits whose clusters are all resident at once
     for (int c = s; c >= 2; --c) {
-      if (reduce_bytes(p.bn, c) <= pipeline_bytes(p.bn) && max_clusters_bn(p.bn, c) >= tiles) {
+      if (max_clusters_bn(p.bn, c) >= tiles) {
         p.S = c;
         p.cluster = true;
         break;
@@ -475,8 +419,8 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
   int st;
 #define MOE_TC_CASE(B)                                                                                   \
   case B:                                                                                                 \
-    st = p.cluster ? launch_bn<B, true>(x, w, dst, T, H, E, p, err, stream)                             \
-                   : launch_bn<B, false>(x, w, dst, T, H, E, p, err, stream);                            \
+    st = p.cluster ? launch_bn<B, true>(x, w, dst, part, T, H, E, p, err, stream)                       \
+                   : launch_bn<B, false>(x, w, dst, part, T, H, E, p, err, stream);                      \
     break;
   switch (p.bn) {
     MOE_TC_CASE(16)
@@ -484,8 +428,8 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
     MOE_TC_CASE(64)
     MOE_TC_CASE(128)
     default:
-      st = p.cluster ? launch_bn<256, true>(x, w, dst, T, H, E, p, err, stream)
-                     : launch_bn<256, false>(x, w, dst, T, H, E, p, err, stream);
+      st = p.cluster ? launch_bn<256, true>(x, w, dst, part, T, H, E, p, err, stream)
+                     : launch_bn<256, false>(x, w, dst, part, T, H, E, p, err, stream);
       break;
   }
 #undef MOE_TC_CASE
