@@ -10,15 +10,19 @@
 //
 // GB300 design: one CTA of 4 warps per token. Thread i holds the experts i + 128 j
 // (j < NJ), so each load instruction of a warp reads 128 contiguous bytes of the
-// logits row. Selection does not run K serial argmax rounds: the K-th largest of the
-// 128 thread maxima is a lower bound of the K-th largest key (K different threads
-// hold a key at least that large). Each warp sorts its 32 maxima with a bitonic
-// network over shuffles; two rounds of bitonic merging of the four sorted lists give
-// the top 32 of all 128 maxima, whose K-th entry is the bound. The few candidates at
-// or above it (about 17 of 896 for random scores) are compacted into shared memory;
-// up to 32 of them are ordered by one warp-wide bitonic sort of (key, ~expert), so
-// lane k holds slot k (32 < count <= 64: ranked by counting; more, from heavy ties:
-// K rounds of argmax).
+// logits row. Selection runs in two tiers. Every expert first gets an approximate key
+// (the hardware's approximate exp2 and reciprocal: within 1.79e-7 of the specified
+// sigmoid over all inputs). The K-th largest of the 128 thread maxima is a lower bound
+// of the K-th largest key (K different threads hold a key at least that large): each
+// warp sorts its 32 maxima with a bitonic network over shuffles, and two rounds of
+// bitonic merging of the four sorted lists give the top 32 of all 128. Every expert
+// whose approximate key is within a margin of that bound (about 17 of 896 for random
+// scores) is a candidate -- the margin covers twice the approximation error, so the
+// exact top K are among them. Only the candidates get the specified sigmoid and their
+// exact keys; up to 32 are ranked by one warp (each lane counts the candidates whose
+// (key, ~expert) orders before its own: 32 independent comparisons), 32 < count <= 64
+// by counting over shared memory, more (heavy ties) by exact keys for all and K rounds
+// of argmax. The result is that of the exact keys, bit for bit.
 #include "topk.cuh"
 
 namespace moe {

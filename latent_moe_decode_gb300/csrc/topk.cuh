@@ -224,26 +224,31 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
       const uint32_t k = exact(l_s[lane], __uint_as_float(l_key[lane]), &cs);
       c = ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)l_e[lane]);
     }
+    // slot of each candidate = how many candidates order before it (keys distinct with the
+    // expert in the low word): 32 independent comparisons instead of a sorting network
+    int rank = 0;
 #pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const unsigned long long oc = __shfl_xor_sync(kFull, c, j);
-        const float os = __shfl_xor_sync(kFull, cs, j);
-        const bool descending = (lane & k) == 0;
-        const bool keep_max = ((lane & j) == 0) == descending;
-        const bool take = keep_max ? (oc > c) : (oc < c);
-        c = take ? oc : c;
-        cs = take ? os : cs;
-      }
+    for (int j = 0; j < 32; ++j) rank += __shfl_sync(kFull, c, j) > c;
+    if (lane < total && rank < K) {
+      slot_id[rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
+      slot_s[rank] = cs;
     }
+    __syncwarp();
+    // weights: unbiased scores over their slot-order FP32 sum (all loads first, then the
+    // sum in order)
+    float sc[MOE_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k) sc[k] = k < K ? slot_s[k] : 0.f;
     float S = 0.f;
-    for (int k = 0; k < K; ++k) S = __fadd_rn(S, __shfl_sync(kFull, cs, k));
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k)
+      if (k < K) S = __fadd_rn(S, sc[k]);
     if (lane < K) {
-      float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(cs, S)) : cs;
+      const float sv = slot_s[lane];
+      float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(sv, S)) : sv;
       if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
       const size_t o = (size_t)t * K + lane;
-      a.ids[o] = (int32_t)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
+      a.ids[o] = slot_id[lane];
       if (a.weights) a.weights[o] = w;
       if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
     }
