@@ -134,9 +134,11 @@ class Step:
     """Device-resident inputs and preallocated buffers of one routing-and-combine step,
     plus the step captured as a CUDA graph. With nsets > 1 the inputs are held in
     nsets separate copies (same values, distinct memory), each with its own buffers and
-    graph, so that steps run back to back in turn find their inputs cold in L2."""
+    graph, so that steps run back to back in turn find their inputs cold in L2; with
+    chain > 1, one more graph holds `chain` consecutive steps (one per copy in turn), as
+    a decode loop captures consecutive layers in one graph."""
 
-    def __init__(self, T, device, seed=0, skew=False, router_algo=0, graph=True, nsets=1):
+    def __init__(self, T, device, seed=0, skew=False, router_algo=0, graph=True, nsets=1, chain=1):
         import torch
 
         import latent_moe_decode_gb300 as m
@@ -166,6 +168,13 @@ class Step:
                 with torch.cuda.graph(g):
                     self.run_direct(i)
                 self.graphs.append(g)
+            self.chain_graph, self.chain = None, chain
+            if chain > 1:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(chain):
+                        self.run_direct(i)
+                self.chain_graph = g
 
     def run_direct(self, i=0):
         st = self.sets[i % self.nsets]
@@ -242,6 +251,7 @@ def whole_job_rate(T, world, ms):
 
 
 COLD_FACTOR = 3  # a rotation of input copies moves at least this many L2 capacities
+STEPS_PER_GRAPH = 12  # consecutive steps (layers) one CUDA graph holds in the timed run
 L2_BYTES = 129 << 20
 
 
@@ -310,7 +320,7 @@ def run_ours(args, rank, world, local_rank):
     m.load()
     T = T_WIDE
     nsets = n_copies(chain_bytes(algorithmic_bytes(T)))
-    step = Step(T, dev, seed=rank, nsets=nsets)
+    step = Step(T, dev, seed=rank, nsets=nsets, chain=STEPS_PER_GRAPH)
     rf = step.rf
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -322,6 +332,8 @@ def run_ours(args, rank, world, local_rank):
 
     for i in range(args.warmup * nsets):
         step.run(i)
+    for _ in range(args.warmup):
+        step.chain_graph.replay()
     barrier()
     rot, copies = rotations(step, args.steps)
     for fns in rot.values():
@@ -330,10 +342,13 @@ def run_ours(args, rank, world, local_rank):
     barrier()
 
     with ClockSampler(local_rank) as clk:
-        # (a) K whole steps back to back (one CUDA graph each), rotating over input sets
-        #     that together exceed L2, so every step reads its inputs cold
+        # (a) K whole steps back to back, rotating over input sets that together exceed
+        #     L2 (every step reads its inputs cold): CUDA graphs of STEPS_PER_GRAPH
+        #     consecutive steps, then single-step graphs for the remainder
         barrier()
-        ms = time_back_to_back([lambda i=i: step.run(i) for i in range(args.steps)], stream)
+        full, rest = divmod(args.steps, STEPS_PER_GRAPH)
+        fns = [step.chain_graph.replay] * full + [lambda i=i: step.run(i) for i in range(rest)]
+        ms = time_back_to_back(fns, stream) * len(fns) / args.steps
         barrier()
         # (b) each call alone, K launches back to back over rotated input copies
         per_ms = {k: time_back_to_back(fns, stream) for k, fns in rot.items()}
@@ -427,8 +442,9 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: steps run back to back over {nsets} copies of the inputs "
                          f"({nsets * chain_bytes(ab) / 1e6:.0f} MB in rotation > 129 MB L2), so each step reads them cold; "
                          f"each call alone likewise over {copies} copies",
-                   "launch": "each step one CUDA graph (replayed back to back), programmatic dependent launch "
-                             "between its kernels",
+                   "launch": f"CUDA graphs of {STEPS_PER_GRAPH} consecutive steps (as a decode loop captures "
+                             "consecutive layers), replayed back to back; programmatic dependent launch between "
+                             "the kernels of a step",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "chain_GB/s": round(chain_bytes(ab) / (ms * 1e-3) / 1e9, 1),
         "ms_per_step_flushed": round(flushed_ms, 5),
@@ -450,7 +466,7 @@ def run_ours(args, rank, world, local_rank):
 
 def run_sweep(args):
     """The skew sweep: the whole step per T with Zipf(1.1) expert popularity, plus each
-    call alone; one JSON line per T."""
+    call alone and the stock router; one JSON line per T."""
     import torch
 
     import latent_moe_decode_gb300 as m
@@ -462,28 +478,38 @@ def run_sweep(args):
     hbm = load_peaks()[0]
     for T in [int(t) for t in args.sweep.split(",")]:
         for algo in ([0] if not args.router_algos else [int(a) for a in args.router_algos.split(",")]):
-            step = Step(T, dev, skew=True, router_algo=algo)
-            for _ in range(args.warmup):
-                step.run()
-            ms = float(np.mean(time_region(step.run, args.steps, flush, stream)))
-            per = {k: round(float(np.mean(time_region(fn, args.steps, flush, stream))) * 1e3, 2) for k, fn in step.calls().items()}
+            ab = algorithmic_bytes(T)
+            nsets = n_copies(chain_bytes(ab))
+            step = Step(T, dev, skew=True, router_algo=algo, nsets=nsets)
+            for i in range(args.warmup * nsets):
+                step.run(i)
+            # K steps back to back over input copies larger than L2, as the main line
+            ms = time_back_to_back([lambda i=i: step.run(i) for i in range(args.steps)], stream)
+            rot, _ = rotations(step, args.steps)
+            per = {k: round(time_back_to_back(fns, stream) * 1e3, 2) for k, fns in rot.items()}
             stock = None
-            try:  # the stock router call of the pages (cuBLAS through torch), for context
+            try:  # the stock router call (cuBLAS through torch), timed the same way, for context
+                nr = n_copies(ab["router"])
+                xs = [step.x] + [step.x.clone() for _ in range(nr - 1)]
+                ws = [step.w] + [step.w.clone() for _ in range(nr - 1)]
                 out = torch.empty(T, synth.E, dtype=torch.float32, device=dev)
-                mm = lambda: torch.mm(step.x, step.w.t(), out_dtype=torch.float32, out=out)
-                mm()
-                stock = round(float(np.mean(time_region(mm, args.steps, flush, stream))) * 1e3, 2)
+                mms = [lambda i=i: torch.mm(xs[i % nr], ws[i % nr].t(), out_dtype=torch.float32, out=out)
+                       for i in range(args.steps)]
+                mms[0]()
+                stock = round(time_back_to_back(mms, stream) * 1e3, 2)
+                del xs, ws
             except Exception:
                 pass
             loads = np.bincount(step.rf.ids.cpu().numpy().ravel(), minlength=synth.E)
-            ab = algorithmic_bytes(T)
             print(json.dumps({"T": T, "router_algo": algo, "us_per_step": round(ms * 1e3, 2),
                               "tokens/s": round(T / (ms * 1e-3), 1), "chain_GB/s": round(chain_bytes(ab) / (ms * 1e-3) / 1e9, 1),
                               "frac_hbm_chain": round(chain_bytes(ab) / (ms * 1e-3) / 1e9 / hbm, 3), "us_alone": per,
                               "us_stock_router_torch_mm": stock,
-                              "expert_load_max_over_mean": round(float(loads.max() / max(loads.mean(), 1e-9)), 2)}), flush=True)
+                              "expert_load_max_over_mean": round(float(loads.max() / max(loads.mean(), 1e-9)), 2),
+                              "timing": "back to back over input copies larger than L2 (cold inputs every launch)"}),
+                  flush=True)
             assert m.device_error(clear=True) == 0
-            del step
+            del step, rot
             torch.cuda.empty_cache()
 
 

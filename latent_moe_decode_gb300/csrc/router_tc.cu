@@ -322,15 +322,17 @@ int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, float* part, int
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<BN>::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = CLUSTER ? p.S : 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  // No programmatic dependent launch for the router itself: launched early, its CTAs
+  // (a whole SM's shared memory each) only contended with the preceding kernel for
+  // SMs; measured, a chain of steps ran about 4 us a step faster without it. (The
+  // kernels after the router still launch early: it signals them.)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER ? p.S : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CLUSTER ? 2 : 1;
+  cfg.numAttrs = CLUSTER ? 1 : 0;
   const int discard = (reinterpret_cast<uintptr_t>(part) & 127u) == 0 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, dst, part, T, E, p.n_kb, p.S, discard, err) == cudaSuccess
              ? MOE_OK
