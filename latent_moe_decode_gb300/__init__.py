@@ -264,9 +264,8 @@ def route_finalize(x, w, bias, latent, rows, K: int, renormalize: bool, scale: f
 class RouteFinalize:
     """The whole routing-and-combine step, with its buffers preallocated:
     router logits -> sigmoid+bias top-K with the MXFP8 latent in the same launch ->
-    routing lists -> Finalize, on one stream. (Finalize does not read the lists, but
-    beside it the lists kernel, latency-bound, waits behind Finalize's HBM stream and
-    leaves Finalize's SMs unevenly loaded: in sequence the step is shorter.)
+    routing lists -> Finalize, on one stream (Finalize does not read the lists and
+    starts streaming its rows while they are built).
 
     ``run()`` launches the library's kernels (programmatic dependent launch between
     consecutive kernels of a stream) and allocates nothing, so it can be captured in a

@@ -1,6 +1,9 @@
 // The routing-and-combine step as one call: the four launches of the chain, in order,
-// on the caller's stream (each kernel waits for its predecessor with programmatic
-// dependent launch, so the launches overlap their prologues).
+// on the caller's stream. The router is launched the ordinary way (it starts once its
+// predecessor has completed) and signals its dependents after that; the later kernels
+// use programmatic dependent launch and wait for their predecessor only before reading
+// what the chain wrote -- the MXFP8 CTAs (a step input) not at all, Finalize only at
+// its end, so it streams its rows while the lists kernel runs.
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideMoE.run
 // (router -> route -> Finalize on one stream) and ...moe.ep.layer, EpMoeLayer.__call__.

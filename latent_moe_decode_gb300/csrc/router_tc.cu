@@ -109,7 +109,7 @@ __device__ __forceinline__ void cluster_sync() {
 // chunks [first(r), first(r + 1)).
 __host__ __device__ constexpr int chunk_first(int r, int nch, int S) { return (r * nch) / S; }
 
-// CLUSTER: the S split CTAs of a tile form one cluster and reduce through DSMEM.
+// CLUSTER: the S split CTAs of a tile form one cluster and reduce in this kernel.
 template <int BN, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, float* out,

@@ -1,6 +1,6 @@
-"""The whole routing-and-combine step on one stream (router -> top-16 -> lists ||
-MXFP8 -> Finalize, programmatic dependent launches between the kernels) against the
-oracle, at the decode shapes: logits within tolerance, everything else bit for bit,
+"""The whole routing-and-combine step on one stream (router -> top-16 with the MXFP8
+latent in the same launch -> lists -> Finalize, programmatic dependent launches between
+the kernels) against the oracle, at the decode shapes: logits within tolerance, everything else bit for bit,
 with the oracle's top-k consuming the GPU's logits."""
 import numpy as np
 import pytest
