@@ -513,6 +513,58 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+def front_flops_bytes(T, H=synth.H, E=synth.E, L=synth.L):
+    """Algorithmic FLOPs and bytes of the front projection: x and both weights read
+    once, FP32 logits and BF16 latent written once."""
+    return 2.0 * T * (E + L) * H, 2.0 * T * H + 2.0 * (E + L) * H + 4.0 * T * E + 2.0 * T * L
+
+
+def run_front(args):
+    """The front projection (router logits + latent down projection in one launch), one
+    JSON line per T: back to back over input copies larger than L2, against the
+    measured bf16 tensor peak, with the two stock torch.mm calls for context."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    stream = torch.cuda.current_stream()
+    hbm, tflops = load_peaks()[:2]
+    wr = torch.from_numpy(synth.router_weight().view(np.int16)).view(torch.bfloat16).to(dev)
+    wd = torch.from_numpy(synth.latent_down_weight().view(np.int16)).view(torch.bfloat16).to(dev)
+    for T in [int(t) for t in args.front.split(",")]:
+        x = torch.from_numpy(synth.hidden_rows(T).view(np.int16)).view(torch.bfloat16).to(dev)
+        fl, by = front_flops_bytes(T)
+        n = n_copies(int(by))
+        xs, wrs, wds = [x] + [x.clone() for _ in range(n - 1)], [wr] + [wr.clone() for _ in range(n - 1)], \
+            [wd] + [wd.clone() for _ in range(n - 1)]
+        logits = torch.empty(T, synth.E, dtype=torch.float32, device=dev)
+        latent = torch.empty(T, synth.L, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(1, m.front_projection_workspace(T, synth.H, synth.E, synth.L)), dtype=torch.uint8, device=dev)
+        calls = [lambda i=i: m.front_projection(xs[i % n], wrs[i % n], wds[i % n], logits=logits, latent=latent,
+                                                workspace=ws) for i in range(args.steps)]
+        for c in calls[: max(args.warmup, n)]:
+            c()
+        ms = time_back_to_back(calls, stream)
+        stock = [lambda i=i: (torch.mm(xs[i % n], wrs[i % n].t(), out_dtype=torch.float32, out=logits),
+                              torch.mm(xs[i % n], wds[i % n].t(), out=latent)) for i in range(args.steps)]
+        for c in stock[: max(args.warmup, n)]:
+            c()
+        ms_stock = time_back_to_back(stock, stream)
+        ach = fl / (ms * 1e-3) / 1e12
+        print(json.dumps({"T": T, "us": round(ms * 1e3, 2), "TFLOP/s": round(ach, 1), "peak_TFLOP/s": tflops,
+                          "frac_tensor": round(ach / tflops, 3), "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(by / (ms * 1e-3) / 1e9 / hbm, 3),
+                          "us_stock_two_torch_mm": round(ms_stock * 1e3, 2), "GFLOP": round(fl / 1e9, 2),
+                          "MB": round(by / 1e6, 2),
+                          "timing": "back to back over input copies larger than L2 (cold inputs every launch)"}),
+              flush=True)
+        assert m.device_error(clear=True) == 0
+        del xs, wrs, wds
+        torch.cuda.empty_cache()
+
+
 def run_ncu_step(args):
     """The wide step, untimed, warmup + steps times (for profiler captures)."""
     import torch
@@ -521,6 +573,22 @@ def run_ncu_step(args):
     step = Step(args.T or T_WIDE, dev, graph=False, router_algo=args.router_algo)
     for _ in range(args.warmup + args.steps):
         step.run()
+    torch.cuda.synchronize()
+
+
+def run_ncu_front(args):
+    """The front projection at T (default 1020), untimed, warmup + steps times."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    T = args.T or T_WIDE
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    x, wr, wd = bf(synth.hidden_rows(T)), bf(synth.router_weight()), bf(synth.latent_down_weight())
+    for _ in range(args.warmup + args.steps):
+        m.front_projection(x, wr, wd)
     torch.cuda.synchronize()
 
 
@@ -585,6 +653,8 @@ def main():
     ap.add_argument("--sweep", default=None, help="comma-separated T list: the skew sweep, one JSON line per T")
     ap.add_argument("--router-algos", default=None, help="with --sweep: router kernel families to time (0 auto, 1 simt, 2 tcgen05)")
     ap.add_argument("--ncu-step", action="store_true", help="run the step untimed (for profiler captures)")
+    ap.add_argument("--front", default=None, help="comma-separated T list: time the front projection, one JSON line per T")
+    ap.add_argument("--ncu-front", action="store_true", help="run the front projection untimed (for profiler captures)")
     ap.add_argument("--T", type=int, default=0, help="with --ncu-step: token count (default 1020)")
     ap.add_argument("--router-algo", type=int, default=0, help="with --ncu-step: router kernel family")
     args = ap.parse_args()
@@ -595,6 +665,12 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.ncu_step:
         run_ncu_step(args)
+        return
+    if args.ncu_front:
+        run_ncu_front(args)
+        return
+    if args.front:
+        run_front(args)
         return
     if args.sweep:
         run_sweep(args)

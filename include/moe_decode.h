@@ -131,6 +131,38 @@ int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, float* logit
                               moe_stream_t stream);
 
 /* -------------------------------------------------------------------------------
+ * Front projection: the router logits and the latent down projection of the same
+ * hidden rows in one tensor-core launch (one pass over x for both weights).
+ *   logits[t, e] = sum_j x[t, j] * w_router[e, j]                 FP32 [T, E]
+ *   latent[t, l] = bf16_rn( sum_j x[t, j] * w_down[l, j] )        BF16 [T, L]
+ * Source: [wide] module docstring ("front one FP32-out GEMM over this rank's router
+ * rows and latent down shard"; precision: "FP32 router logits, the latent rounded once
+ * to BF16 (as the stock GEMM epilogue)"); [wide] WideMoE.__init__ (`packed`: the
+ * router rows stacked on the latent down rows); [ep] EpMoeLayer.stock_order
+ * (front = mm(x, front^T), the latent its last 3584 columns, BF16).
+ *
+ *   x         device, BF16 [T, H]        hidden rows
+ *   w_router  device, BF16 [E, H]        router weight (gate)
+ *   w_down    device, BF16 [L, H]        latent down projection
+ *   logits    device, FP32 [T, E]        output
+ *   latent    device, BF16 [T, L]        output
+ *   workspace device scratch of at least moe_front_projection_workspace(T, H, E, L)
+ *             bytes (NULL allowed when that is 0); clobbered. Calls that share a
+ *             workspace must not overlap.
+ * Requirements: T, E, L >= 1, H >= 8, H % 8 == 0 (MOE_ERR_INVALID_ARGUMENT);
+ * E + L < 2^24 (MOE_ERR_CAPACITY); x, w_router, w_down 16-byte aligned, logits 4-byte,
+ * latent 2-byte (MOE_ERR_ALIGNMENT).
+ * Numerics: each output is an FP32 tensor-core sum of exact BF16 products, split-K
+ * partials (if any) reduced in a fixed order: deterministic, within 1e-5 *
+ * sum_j |x w| of the exact sum before the latent's one round-to-nearest-even to BF16.
+ * The logits need not be bit-identical to moe_router_logits (another split plan).
+ * ------------------------------------------------------------------------------- */
+size_t moe_front_projection_workspace(int T, int H, int E, int L);
+int moe_front_projection(const uint16_t* x, const uint16_t* w_router, const uint16_t* w_down, float* logits,
+                         uint16_t* latent, int T, int H, int E, int L, void* workspace, size_t workspace_bytes,
+                         moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
  * Sigmoid + e_score_correction_bias top-K with renormalised weights.
  * Source: [ep] EpMoeLayer.topk (one group, sigmoid scoring, correction bias,
  * renormalize, routed scaling); [wide] WideRoute docstring ("exact top16 and

@@ -17,7 +17,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MoeError", "load", "router_logits", "router_logits_workspace", "topk_route",
+    "MoeError", "load", "router_logits", "router_logits_workspace", "front_projection",
+    "front_projection_workspace", "topk_route",
     "build_routing_lists", "build_routing_lists_workspace", "mxfp8_quantize_rows",
     "finalize", "route_finalize", "route_finalize_workspace", "device_error", "RouteFinalize",
     "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05",
@@ -39,6 +40,8 @@ SIGNATURES = {
     "moe_router_logits": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "moe_router_logits_ex": (_I, [_P, _P, _P, _I, _I, _I, _P, _SZ, _I, _P]),
     "moe_router_logits_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "moe_front_projection_workspace": (_SZ, [_I, _I, _I, _I]),
+    "moe_front_projection": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_topk_route": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "moe_topk_route_quantize": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "moe_build_routing_lists_workspace": (_SZ, [_I, _I, _I]),
@@ -127,6 +130,29 @@ def router_logits(x, w, out=None, workspace=None, algo: int = ROUTER_AUTO, strea
     _check("moe_router_logits_ex", load().moe_router_logits_ex(
         _ptr(x), _ptr(w), _ptr(out), T, H, E, _ptr(workspace), wb, algo, _stream(stream)))
     return out
+
+
+def front_projection_workspace(T: int, H: int, E: int, L: int) -> int:
+    return int(load().moe_front_projection_workspace(T, H, E, L))
+
+
+def front_projection(x, w_router, w_down, logits=None, latent=None, workspace=None, stream=None):
+    """(FP32 logits [T, E] = x @ w_router^T, BF16 latent [T, L] = bf16(x @ w_down^T)), one launch."""
+    T, H = x.shape
+    E, L = w_router.shape[0], w_down.shape[0]
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(w_router, torch.bfloat16, (E, H), "w_router")
+    _need(w_down, torch.bfloat16, (L, H), "w_down")
+    logits = _empty((T, E), torch.float32, x) if logits is None else _need(logits, torch.float32, (T, E), "logits")
+    latent = _empty((T, L), torch.bfloat16, x) if latent is None else _need(latent, torch.bfloat16, (T, L), "latent")
+    need = front_projection_workspace(T, H, E, L)
+    if need and workspace is None:
+        workspace = _empty((need,), torch.uint8, x)
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_front_projection", load().moe_front_projection(
+        _ptr(x), _ptr(w_router), _ptr(w_down), _ptr(logits), _ptr(latent), T, H, E, L, _ptr(workspace), wb,
+        _stream(stream)))
+    return logits, latent
 
 
 def topk_route(logits, bias, K: int, renormalize: bool = True, scale: float = 1.0,

@@ -16,6 +16,7 @@ struct TcPlan {
   int S;     // K splits
   int n_kb;  // 64-wide K blocks
   bool cluster;  // the S splits of a tile form a cluster and reduce in one kernel (partials through L2)
+  bool pair = false;  // CTA pairs (cta_group::2 MMAs over 256 weight rows); S pairs per cluster
 };
 // Split-K workspace a plan needs (bytes): the partials [S][T][E] of the two-kernel
 // reduction, or, for a cluster plan, every tile's S partial tiles [BN][128].
@@ -28,6 +29,14 @@ inline size_t tc_workspace(const TcPlan& p, int T, int E) {
 TcPlan tc_plan(int T, int H, int E, int sm_count);
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,
                      float* part, uint32_t* err, cudaStream_t stream);
+
+// The front projection: router logits (FP32 [T, E]) and the latent down projection
+// (BF16 [T, L], one rounding of the FP32 sum) in one tensor-core launch over x. The
+// plan's splits are reduced on chip (cluster plan) or there are none.
+TcPlan front_plan(int T, int H, int E, int L, int sm_count);
+size_t front_workspace(const TcPlan& p, int T, int E, int L);
+int launch_front_tc(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* logits, uint16_t* latent, int T,
+                    int H, int E, int L, const TcPlan& p, float* part, uint32_t* err, cudaStream_t stream);
 
 // logits = sum over s of part[s] (split order), part [S][T][E].
 int launch_router_reduce(const float* part, int S, int T, int E, float* logits, cudaStream_t stream);

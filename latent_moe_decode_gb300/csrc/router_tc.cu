@@ -48,10 +48,13 @@ constexpr int kBK = 64;               // K elements per stage (128 bytes: one sw
 constexpr int kThreads = 512;         // 16 warps: two lanes run the mainloop, all sixteen the epilogue
 constexpr int kGroups = kThreads / 128;  // warpgroups: each reaches all 128 TMEM lanes
 
-template <int BN>
+// PAIR: two CTAs (one SM each) run one M = 256 MMA (cta_group::2); each stages its
+// own 128 weight rows and half of the BN token rows.
+template <int BN, bool PAIR = false>
 struct Cfg {
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes < 8 ? (200 * 1024) / kStageBytes : 8;
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
@@ -65,6 +68,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same for a CTA pair: `bar` is a shared::cluster address that may lie in the
+// peer CTA (the pair's leader counts both CTAs' bytes on one barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Shared::cluster address of the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 // Shared-memory matrix descriptor: K-major tile of 128-byte rows, 128-byte swizzle,
 // 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -76,9 +101,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: BF16 x BF16 -> FP32, both K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t instr_desc(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// Instruction descriptor: BF16 x BF16 -> FP32, both K-major, M = m (128, or 256 for a
+// CTA pair), N = n.
+__host__ __device__ constexpr uint32_t instr_desc(int n, int m = kBM) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
@@ -89,6 +115,22 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// CTA pair: M = 256 over both CTAs' weight rows, N = BN over both CTAs' token rows;
+// issued by the leader, each CTA's TMEM receives its 128 rows.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
+}
+
+// CTA pair: arrive on the barrier at this shared-memory offset in every CTA of `mask`
+// (cluster ranks) once the leader's MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+               "h"(mask)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -109,15 +151,41 @@ __device__ __forceinline__ void cluster_sync() {
 // chunks [first(r), first(r + 1)).
 __host__ __device__ constexpr int chunk_first(int r, int nch, int S) { return (r * nch) / S; }
 
+// Output of one logit (or latent) value: expert tiles (mt < mt1) store FP32 logits
+// [T, E]; with FRONT, the tiles past them are rows of the second weight and store the
+// latent [T, L] rounded once to BF16 (round to nearest even).
+template <bool FRONT>
+__device__ __forceinline__ void store_out(float* out, uint16_t* out2, int t, int mt, int mt1, int row, int E, int L,
+                                          float v) {
+  if (!FRONT || mt < mt1) {
+    const int e = mt * kBM + row;
+    if (e < E) out[(size_t)t * E + e] = v;
+  } else {
+    const int l = (mt - mt1) * kBM + row;
+    if (l < L) out2[(size_t)t * L + l] = f32_to_bf16(v);
+  }
+}
+
 // CLUSTER: the S split CTAs of a tile form one cluster and reduce in this kernel.
-template <int BN, bool CLUSTER>
+// FRONT: the tiles mt >= mt1 stream a second weight (tm_w2, the latent down
+// projection) and write BF16 rows of `out2`: one launch for both GEMMs that read x.
+// PAIR: CTAs 2s and 2s + 1 of a cluster are a pair that computes 256 weight rows x BN
+// tokens with cta_group::2 MMAs (blockIdx.z counts pairs of 128-row tiles). Each CTA
+// loads its 128 weight rows and BN/2 token rows; both CTAs' copies complete on the
+// leader's (even CTA's) full barrier, the leader issues the MMAs, and its commits
+// arrive on the empty and accumulator barriers of both CTAs. A pair reads half the
+// token bytes per SM of two single CTAs for the same MMA work.
+template <int BN, bool CLUSTER, bool FRONT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-    router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, float* out,
-                     float* part, int T, int E, int n_kb, int S, int discard, uint32_t* err) {
-  using C = Cfg<BN>;
+    router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_w2, float* out, uint16_t* out2, float* part, int T, int E,
+                     int L, int mt1, int n_kb, int S, int discard, uint32_t* err) {
+  using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int s = blockIdx.x, nt = blockIdx.y, mt = blockIdx.z;
+  const int h = PAIR ? (int)(blockIdx.x & 1u) : 0;  // pair half (cluster rank parity)
+  const int s = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x, nt = blockIdx.y;
+  const int mt = PAIR ? 2 * (int)blockIdx.z + h : (int)blockIdx.z;  // this CTA's 128-row tile
   const int kb0 = (int)(((long long)s * n_kb) / S), kb1 = (int)(((long long)(s + 1) * n_kb) / S);
   const int nkb = kb1 - kb0;
 
@@ -138,40 +206,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+    if (FRONT) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w2)) : "memory");
   }
   if (warp == 2) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(C::kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if constexpr (PAIR) {  // one warp of each CTA of the pair, collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(C::kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(C::kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // the peer's barriers are initialised before any copy may complete on them
+  else
+    __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *slot_ptr;
 
-  grid_wait();
-  grid_launch_dependents();  // after the wait: dependents may rely on all before the router  // x (and the gate) may be written by the preceding kernel
+  grid_wait();                // x (and the weights) may be written by the preceding kernel
+  grid_launch_dependents();   // after the wait: dependents may rely on all before this kernel
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
+      const CUtensorMap* wmap = (FRONT && mt >= mt1) ? &tm_w2 : &tm_w;
+      const int wrow = ((FRONT && mt >= mt1) ? mt - mt1 : mt) * kBM;
+      const int xrow = nt * BN + h * C::kBRows;
+      // a pair's copies complete on the leader's barrier, which expects both CTAs' bytes
+      const uint32_t lead = PAIR ? (cluster_rank() & ~1u) : 0u;
       int issued = 0;
       for (int i = 0; i < nkb; ++i) {
         const int st = i % C::kStages;
         const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
         if (!mbar_wait(empty(st), ph ^ 1u, err)) break;
         const uint32_t a_dst = base + st * C::kStageBytes;
-        mbar_expect_tx(full(st), C::kStageBytes);
-        tma_load_2d(a_dst, &tm_w, (kb0 + i) * kBK, mt * kBM, full(st));
-        tma_load_2d(a_dst + C::kABytes, &tm_x, (kb0 + i) * kBK, nt * BN, full(st));
+        if constexpr (PAIR) {
+          const uint32_t fb = map_rank(full(st), lead);
+          if (h == 0) mbar_expect_tx(full(st), 2 * C::kStageBytes);
+          tma_load_2d_pair(a_dst, wmap, (kb0 + i) * kBK, wrow, fb);
+          tma_load_2d_pair(a_dst + C::kABytes, &tm_x, (kb0 + i) * kBK, xrow, fb);
+        } else {
+          mbar_expect_tx(full(st), C::kStageBytes);
+          tma_load_2d(a_dst, wmap, (kb0 + i) * kBK, wrow, full(st));
+          tma_load_2d(a_dst + C::kABytes, &tm_x, (kb0 + i) * kBK, xrow, full(st));
+        }
         ++issued;
       }
-      // our copies still in flight land before the CTA may exit
-      const int first = issued > C::kStages ? issued - C::kStages : 0;
-      for (int i = first; i < issued; ++i) mbar_wait(full(i % C::kStages), (uint32_t)(i / C::kStages) & 1u, err);
+      // our copies still in flight land before the CTA may exit (a pair's peer: its
+      // copies complete on the leader's barriers, which the leader's MMA waits for)
+      if (h == 0) {
+        const int first = issued > C::kStages ? issued - C::kStages : 0;
+        for (int i = first; i < issued; ++i) mbar_wait(full(i % C::kStages), (uint32_t)(i / C::kStages) & 1u, err);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer
-      constexpr uint32_t idesc = instr_desc(BN);
+    if (lane == 0 && h == 0) {  // MMA issuer (a pair's leader)
+      constexpr uint32_t idesc = instr_desc(BN, PAIR ? 2 * kBM : kBM);
+      const uint16_t pair_mask = PAIR ? (uint16_t)(3u << (cluster_rank() & ~1u)) : (uint16_t)0;
       for (int i = 0; i < nkb; ++i) {
         const int st = i % C::kStages;
         if (!mbar_wait(full(st), (uint32_t)(i / C::kStages) & 1u, err)) break;
@@ -179,15 +272,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_addr = base + st * C::kStageBytes;
         const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          mma_bf16(tmem, sw128_desc(a_addr + 32u * k), sw128_desc(b_addr + 32u * k), idesc, (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(empty(st));
+        for (int k = 0; k < kBK / 16; ++k) {
+          if constexpr (PAIR)
+            mma_bf16_pair(tmem, sw128_desc(a_addr + 32u * k), sw128_desc(b_addr + 32u * k), idesc, (i > 0 || k > 0) ? 1u : 0u);
+          else
+            mma_bf16(tmem, sw128_desc(a_addr + 32u * k), sw128_desc(b_addr + 32u * k), idesc, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        if constexpr (PAIR)
+          mma_commit_pair(empty(st), pair_mask);
+        else
+          mma_commit(empty(st));
       }
-      mma_commit(accum);
+      if constexpr (PAIR)
+        mma_commit_pair(accum, pair_mask);
+      else
+        mma_commit(accum);
     }
     __syncwarp();
   }
-
   // epilogue: TMEM lane = expert row, column = token
   const bool done = __all_sync(0xFFFFFFFFu, mbar_wait(accum, 0, err));  // warp-uniform for tcgen05.ld
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -205,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // in L2 (discard.global.L2), so the scratch is never written back to HBM.
     constexpr int nch = BN / 16;
     const int my0 = chunk_first(s, nch, S), my1 = chunk_first(s + 1, nch, S);
-    const size_t tile = (size_t)mt * gridDim.y + nt;
+    const size_t tile = (size_t)mt * gridDim.y + nt;  // (a pair's two CTAs: two tiles)
     float* slot = part + (tile * S + s) * (size_t)BN * kBM;
     if (done) {
 #pragma unroll 1
@@ -219,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cluster_sync();  // every split's partial chunks are written and visible to the cluster
-    const int e = mt * kBM + row;
     if (done) {
 #pragma unroll 1
       for (int ch = my0 + wg; ch < my1; ch += kGroups) {
@@ -250,35 +351,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
           }
         }
-        if (e < E) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = nt * BN + 16 * ch + j;
-            if (t < T) out[(size_t)t * E + e] = acc[j];
-          }
+        for (int j = 0; j < 16; ++j) {
+          const int t = nt * BN + 16 * ch + j;
+          if (t < T) store_out<FRONT>(out, out2, t, mt, mt1, row, E, L, acc[j]);
         }
       }
     }
   } else if (done) {
-    const int e = mt * kBM + row;
-    float* dst = out + (size_t)s * T * E;
+    float* dst = out + (size_t)s * T * E;  // (FRONT plans have S == 1)
 #pragma unroll 1
     for (int c0 = 16 * wg; c0 < BN; c0 += 16 * kGroups) {
       uint32_t v[16];
       tmem_ld16(tl + (uint32_t)c0, v);
       tmem_wait_ld();
-      if (e < E) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = nt * BN + c0 + j;
-          if (t < T) dst[(size_t)t * E + e] = __uint_as_float(v[j]);
-        }
+      for (int j = 0; j < 16; ++j) {
+        const int t = nt * BN + c0 + j;
+        if (t < T) store_out<FRONT>(dst, out2, t, mt, mt1, row, E, L, __uint_as_float(v[j]));
       }
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+  if constexpr (PAIR) {
+    cluster_sync();  // neither CTA of a pair leaves while the other may still touch its shared memory
+    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+  } else {
+    __syncthreads();
+    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -308,19 +409,25 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool CLUSTER>
-int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, float* part, int T, int H, int E, const TcPlan& p,
-              uint32_t* err, cudaStream_t stream) {
-  CUtensorMap tm_w, tm_x;
-  if (!make_map(&tm_w, w, E, H, kBM) || !make_map(&tm_x, x, T, H, BN)) return MOE_ERR_CUDA;
-  auto kern = router_tc_kernel<BN, CLUSTER>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem) != cudaSuccess)
+// w2 / out2 / L: the second weight of a front launch (FRONT), else unused.
+template <int BN, bool CLUSTER, bool FRONT, bool PAIR>
+int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* dst, uint16_t* out2, float* part, int T,
+              int H, int E, int L, const TcPlan& p, uint32_t* err, cudaStream_t stream) {
+  using C = Cfg<BN, PAIR>;
+  CUtensorMap tm_w, tm_x, tm_w2;
+  if (!make_map(&tm_w, w, E, H, kBM) || !make_map(&tm_x, x, T, H, C::kBRows)) return MOE_ERR_CUDA;
+  if (FRONT ? !make_map(&tm_w2, w2, L, H, kBM) : false) return MOE_ERR_CUDA;
+  if (!FRONT) tm_w2 = tm_w;
+  const int mt1 = (E + kBM - 1) / kBM;
+  const int m_tiles = mt1 + (FRONT ? (L + kBM - 1) / kBM : 0);
+  auto kern = router_tc_kernel<BN, CLUSTER, FRONT, PAIR>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (prefer_max_shared(reinterpret_cast<const void*>(kern)) != MOE_OK) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.S, (T + BN - 1) / BN, (E + kBM - 1) / kBM);
+  cfg.gridDim = PAIR ? dim3(2 * p.S, (T + BN - 1) / BN, (m_tiles + 1) / 2) : dim3(p.S, (T + BN - 1) / BN, m_tiles);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<BN>::kSmem;
+  cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   // No programmatic dependent launch for the router itself: launched early, its CTAs
   // (a whole SM's shared memory each) only contended with the preceding kernel for
@@ -328,32 +435,35 @@ int launch_bn(const uint16_t* x, const uint16_t* w, float* dst, float* part, int
   // kernels after the router still launch early: it signals them.)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CLUSTER ? p.S : 1;
+  attr[0].val.clusterDim.x = PAIR ? 2 * p.S : (CLUSTER ? p.S : 1);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CLUSTER ? 1 : 0;
+  cfg.numAttrs = (CLUSTER || PAIR) ? 1 : 0;
   const int discard = (reinterpret_cast<uintptr_t>(part) & 127u) == 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, dst, part, T, E, p.n_kb, p.S, discard, err) == cudaSuccess
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_w2, dst, out2, part, T, E, L, mt1, p.n_kb, p.S, discard, err) ==
+                 cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
 
-// Clusters of S split CTAs (one tile each) that can be resident at once.
-template <int BN>
+// Clusters of S CTAs (split CTAs of one tile, or pairs of them) that can be resident
+// at once.
+template <int BN, bool PAIR = false>
 int max_clusters(int S) {
   static int cache[9] = {0};
   if (S < 2 || S > 8) return 0;
   if (cache[S]) return cache[S];
-  auto kern = router_tc_kernel<BN, true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem) != cudaSuccess) {
+  auto kern = router_tc_kernel<BN, true, false, PAIR>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN, PAIR>::kSmem) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, 64, 1);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<BN>::kSmem;
+  cfg.dynamicSmemBytes = Cfg<BN, PAIR>::kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
@@ -377,6 +487,15 @@ int max_clusters_bn(int bn, int S) {
     case 64: return max_clusters<64>(S);
     case 128: return max_clusters<128>(S);
     default: return max_clusters<256>(S);
+  }
+}
+
+int max_pair_clusters_bn(int bn, int n_ctas) {
+  switch (bn) {
+    case 32: return max_clusters<32, true>(n_ctas);
+    case 64: return max_clusters<64, true>(n_ctas);
+    case 128: return max_clusters<128, true>(n_ctas);
+    default: return max_clusters<256, true>(n_ctas);
   }
 }
 
@@ -419,24 +538,75 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
   const bool direct = p.S == 1 || p.cluster;
   float* dst = direct ? logits : part;
   int st;
-#define MOE_TC_CASE(B)                                                                                   \
-  case B:                                                                                                 \
-    st = p.cluster ? launch_bn<B, true>(x, w, dst, part, T, H, E, p, err, stream)                       \
-                   : launch_bn<B, false>(x, w, dst, part, T, H, E, p, err, stream);                      \
+#define MOE_TC_CASE(B)                                                                                        \
+  case B:                                                                                                      \
+    st = p.cluster ? launch_bn<B, true, false, false>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream) \
+                   : launch_bn<B, false, false, false>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream); \
     break;
   switch (p.bn) {
     MOE_TC_CASE(16)
     MOE_TC_CASE(32)
     MOE_TC_CASE(64)
     MOE_TC_CASE(128)
-    default:
-      st = p.cluster ? launch_bn<256, true>(x, w, dst, part, T, H, E, p, err, stream)
-                     : launch_bn<256, false>(x, w, dst, part, T, H, E, p, err, stream);
-      break;
+    MOE_TC_CASE(256)
+    default: return MOE_ERR_INVALID_ARGUMENT;
   }
 #undef MOE_TC_CASE
   if (st != MOE_OK || direct) return st;
   return launch_router_reduce(part, p.S, T, E, logits, stream);
+}
+
+// The front launch runs CTA pairs over pairs of 128-row tiles (both weights' tiles in
+// one sequence: a pair may hold the last router tile and the first latent tile). Its
+// splits are reduced only on chip: a cluster of S pairs, or no split.
+TcPlan front_plan(int T, int H, int E, int L, int sm_count) {
+  TcPlan p;
+  p.pair = true;
+  p.bn = 256;
+  for (int b : {32, 64, 128, 256})  // (a pair's MMA takes N >= 32)
+    if (b >= T) {
+      p.bn = b;
+      break;
+    }
+  p.n_kb = (H + kBK - 1) / kBK;
+  const int pairs = ((E + kBM - 1) / kBM + (L + kBM - 1) / kBM + 1) / 2;
+  const int tiles = pairs * ((T + p.bn - 1) / p.bn);  // pair tiles
+  int s = sm_count / (2 * (tiles > 0 ? tiles : 1));
+  s = s < 1 ? 1 : s;
+  if (s > 4) s = 4;  // a cluster of S pairs stays within the portable 8 CTAs
+  if (s > p.n_kb / 2) s = p.n_kb / 2 > 0 ? p.n_kb / 2 : 1;
+  p.S = 1;
+  p.cluster = false;
+  for (int c = s; c >= 2; --c) {
+    if (max_pair_clusters_bn(p.bn, 2 * c) >= tiles) {
+      p.S = c;
+      p.cluster = true;
+      break;
+    }
+  }
+  return p;
+}
+
+size_t front_workspace(const TcPlan& p, int T, int E, int L) {
+  const int pairs = ((E + kBM - 1) / kBM + (L + kBM - 1) / kBM + 1) / 2;
+  return tc_workspace(p, T, 2 * pairs * kBM);
+}
+
+int launch_front_tc(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* logits, uint16_t* latent, int T,
+                    int H, int E, int L, const TcPlan& p, float* part, uint32_t* err, cudaStream_t stream) {
+  if ((p.S > 1 && !p.cluster) || !p.pair) return MOE_ERR_INVALID_ARGUMENT;
+#define MOE_TC_CASE(B)                                                                                         \
+  case B:                                                                                                       \
+    return p.cluster ? launch_bn<B, true, true, true>(x, w, w2, logits, latent, part, T, H, E, L, p, err, stream) \
+                     : launch_bn<B, false, true, true>(x, w, w2, logits, latent, part, T, H, E, L, p, err, stream);
+  switch (p.bn) {
+    MOE_TC_CASE(32)
+    MOE_TC_CASE(64)
+    MOE_TC_CASE(128)
+    MOE_TC_CASE(256)
+    default: return MOE_ERR_INVALID_ARGUMENT;
+  }
+#undef MOE_TC_CASE
 }
 
 }  // namespace moe

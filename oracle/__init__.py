@@ -50,6 +50,9 @@ def _load():
         I = ctypes.c_int
         lib.oracle_router_logits.argtypes = [P, P, I, I, I, P, P]
         lib.oracle_router_logits_sampled.argtypes = [P, P, I, I, P, P, P, P]
+        lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_f64_to_bf16_array.argtypes = [P, P, ctypes.c_long]
         lib.oracle_exp_spec.argtypes = [ctypes.c_float]
         lib.oracle_exp_spec.restype = ctypes.c_float
         lib.oracle_sigmoid.argtypes = [ctypes.c_float]
@@ -110,6 +113,21 @@ def router_logits_sampled(x, w, tok, exp_):
     ab = np.empty(n, np.float64)
     _load().oracle_router_logits_sampled(_ptr(x), _ptr(w), x.shape[1], n, _ptr(tok), _ptr(exp_), _ptr(out), _ptr(ab))
     return out, ab
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    """BF16 bits of FP64 values, rounded once (nearest, ties to even)."""
+    v = _c(np.asarray(v, np.float64), np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_f64_to_bf16_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def latent_down(x, w_down, rel_tol=1e-5):
+    """Exact FP64 latent [T, L] = x @ w_down^T, its BF16 rounding, and the BF16 bounds
+    (lo, hi) that any FP32 sum within rel_tol * sum|x w| of exact rounds into."""
+    ref, ab = router_logits(x, w_down)
+    return ref, f64_to_bf16(ref), f64_to_bf16(ref - rel_tol * ab), f64_to_bf16(ref + rel_tol * ab)
 
 
 def exp_spec(y: float) -> float:

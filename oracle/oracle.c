@@ -102,6 +102,37 @@ void oracle_router_logits_sampled(const uint16_t* x, const uint16_t* w, int H, i
 }
 
 /* ------------------------------------------------------------------------- */
+/* Latent down projection: the front GEMM's latent columns.
+ * [wide] module docstring: one front GEMM over the router rows and the latent down
+ * rows, and "the latent rounded once to BF16 (as the stock GEMM epilogue)";
+ * [ep] EpMoeLayer.stock_order: front = mm(x, front^T) in BF16.
+ * The exact sum is oracle_router_logits over the down-projection rows. The one
+ * rounding to BF16 is done here straight from the double (nearest, ties to even):
+ * going through FP32 first would round twice. BF16 keeps 8 significant bits and
+ * FP32's exponent range (normal down to 2^-126, subnormal steps of 2^-133). */
+uint16_t oracle_f64_to_bf16(double v) {
+  if (v != v) return 0x7FC0u;
+  const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);         /* a = m * 2^e2 with m in [0.5, 1): leading bit 2^(e2-1) */
+  int lead = e2 - 1;
+  if (lead < -126) lead = -126; /* below the normal range the step stays 2^-133 */
+  const double step = ldexp(1.0, lead - 7);
+  const double r = nearbyint(a / step) * step; /* a / step is exact; default mode: ties to even */
+  if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u); /* overflow: infinity */
+  const float f = (float)r;                                     /* exact: 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(sign | ((u >> 16) & 0x7FFFu));
+}
+
+void oracle_f64_to_bf16_array(const double* v, uint16_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16(v[i]);
+}
+
+/* ------------------------------------------------------------------------- */
 /* Sigmoid. The pages say only "sigmoid" ([ep] EpMoeLayer.topk, scoring func
  * "sigmoid"); they fix no numerics. Because the selected ids and weights are
  * compared bit for bit, the method's sigmoid is specified here from a published

@@ -18,7 +18,7 @@ import numpy as np
 H, L, E, K = 7168, 3584, 896, 16
 
 # tensor ids of the counter-based streams
-X, W, BIAS, ROWS, LATENT, PERM, WEIGHTS, SHARED, SKEW = 1, 2, 3, 4, 5, 6, 7, 8, 9
+X, W, BIAS, ROWS, LATENT, PERM, WEIGHTS, SHARED, SKEW, W_DOWN, NORM = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11
 
 # Zipf-skew temperature: bias_e = -1.1 * SKEW_TAU * ln(rank_e). Calibrated once by
 # tests/golden/calibrate_skew.py (oracle top-16 over seed-0 inputs at T=4096) so
@@ -69,6 +69,17 @@ def hidden_rows(T: int, seed: int = 0, h: int = H) -> np.ndarray:
 def router_weight(seed: int = 0, e: int = E, h: int = H) -> np.ndarray:
     """gate: BF16 [e, h] ~ N(0, 0.02)."""
     return normal_bf16(seed, W, (e, h), 0.02)
+
+
+def latent_down_weight(seed: int = 0, l: int = L, h: int = H) -> np.ndarray:
+    """latent down projection: BF16 [l, h] ~ N(0, 0.02) (the router weight's scale;
+    the pages give no initialisation)."""
+    return normal_bf16(seed, W_DOWN, (l, h), 0.02)
+
+
+def norm_weight(seed: int = 0, l: int = L) -> np.ndarray:
+    """RMSNorm weight: BF16 [l] ~ 1 + N(0, 0.1) (near one, as a trained norm)."""
+    return f32_to_bf16_bits((1.0 + rng(seed, NORM).standard_normal(l) * 0.1).astype(np.float32))
 
 
 def correction_bias(seed: int = 0, e: int = E) -> np.ndarray:

@@ -85,6 +85,16 @@ def test_validation_before_any_cuda_call(lib):
     assert chain(8, 0, A16) == 1
     assert chain(8, 16, None) == 1
     assert lib.moe_router_logits_ex(P(264), A16, A16, 8, 7168, 896, None, 0, 0, None) == 2
+    front = lambda T, H, E, L, x=A16, wd=A16, lat=A16: lib.moe_front_projection(x, A16, wd, A16, lat, T, H, E, L, None,
+                                                                               0, None)
+    assert front(0, 7168, 896, 3584) == 1
+    assert front(8, 7167, 896, 3584) == 1
+    assert front(8, 7168, 0, 3584) == 1
+    assert front(8, 7168, 896, 0) == 1
+    assert front(8, 7168, 896, 3584, wd=None) == 1
+    assert front(8, 7168, 1 << 23, 1 << 23) == 3
+    assert front(8, 7168, 896, 3584, x=P(264)) == 2
+    assert front(8, 7168, 896, 3584, lat=P(257)) == 2
 
 
 def test_lists_workspace_query(lib):
