@@ -565,6 +565,64 @@ def run_front(args):
         torch.cuda.empty_cache()
 
 
+def run_norm(args):
+    """Finalize with the RMSNorm epilogue (routed latent and its normalised copy), one
+    JSON line per T: back to back over input copies larger than L2, against the
+    measured HBM copy bandwidth, with plain Finalize timed the same way."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    stream = torch.cuda.current_stream()
+    hbm = load_peaks()[0]
+    K, L = synth.K, synth.L
+    g = torch.from_numpy(synth.norm_weight().view(np.int16)).view(torch.bfloat16).to(dev)
+    for T in [int(t) for t in args.norm.split(",")]:
+        rows = torch.from_numpy(synth.expert_rows(T).view(np.int16)).view(torch.bfloat16).to(dev)
+        u = synth.rng(0, synth.WEIGHTS).random((T, K)).astype(np.float32)
+        w = torch.from_numpy(synth.f32_to_bf16_bits(u / u.sum(1, keepdims=True)).view(np.int16)).view(torch.bfloat16).to(dev)
+        by = 2.0 * T * K * L + 2.0 * T * K + 2.0 * L + 2 * 2.0 * T * L
+        n = n_copies(int(by))
+        rs = [rows] + [rows.clone() for _ in range(n - 1)]
+        routed = torch.empty(T, L, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(T, L, dtype=torch.bfloat16, device=dev)
+        calls = [lambda i=i: m.finalize_rmsnorm(rs[i % n], w, T, K, g, routed=routed, out=out) for i in range(args.steps)]
+        plain = [lambda i=i: m.finalize(rs[i % n], w, T, K, out=routed) for i in range(args.steps)]
+        for c in calls[: max(args.warmup, n)] + plain[: max(args.warmup, n)]:
+            c()
+        ms = time_back_to_back(calls, stream)
+        ms_plain = time_back_to_back(plain, stream)
+        gbs = by / (ms * 1e-3) / 1e9
+        print(json.dumps({"T": T, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "peak_GB/s": hbm,
+                          "frac_hbm": round(gbs / hbm, 3), "MB": round(by / 1e6, 2),
+                          "us_finalize_alone": round(ms_plain * 1e3, 2),
+                          "timing": "back to back over input copies larger than L2 (cold inputs every launch)"}),
+              flush=True)
+        assert m.device_error(clear=True) == 0
+        del rs
+        torch.cuda.empty_cache()
+
+
+def run_ncu_norm(args):
+    """Finalize with the RMSNorm epilogue at T (default 1020), untimed."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    T = args.T or T_WIDE
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    rows, g = bf(synth.expert_rows(T)), bf(synth.norm_weight())
+    u = synth.rng(0, synth.WEIGHTS).random((T, synth.K)).astype(np.float32)
+    w = bf(synth.f32_to_bf16_bits(u / u.sum(1, keepdims=True)))
+    for _ in range(args.warmup + args.steps):
+        m.finalize_rmsnorm(rows, w, T, synth.K, g)
+    torch.cuda.synchronize()
+
+
 def run_ncu_step(args):
     """The wide step, untimed, warmup + steps times (for profiler captures)."""
     import torch
@@ -655,6 +713,8 @@ def main():
     ap.add_argument("--ncu-step", action="store_true", help="run the step untimed (for profiler captures)")
     ap.add_argument("--front", default=None, help="comma-separated T list: time the front projection, one JSON line per T")
     ap.add_argument("--ncu-front", action="store_true", help="run the front projection untimed (for profiler captures)")
+    ap.add_argument("--norm", default=None, help="comma-separated T list: time Finalize with the RMSNorm epilogue")
+    ap.add_argument("--ncu-norm", action="store_true", help="run Finalize with the RMSNorm epilogue untimed (profiling)")
     ap.add_argument("--T", type=int, default=0, help="with --ncu-step: token count (default 1020)")
     ap.add_argument("--router-algo", type=int, default=0, help="with --ncu-step: router kernel family")
     args = ap.parse_args()
@@ -671,6 +731,12 @@ def main():
         return
     if args.front:
         run_front(args)
+        return
+    if args.ncu_norm:
+        run_ncu_norm(args)
+        return
+    if args.norm:
+        run_norm(args)
         return
     if args.sweep:
         run_sweep(args)

@@ -54,6 +54,7 @@ typedef struct CUstream_st* moe_stream_t;
 #define MOE_DEVERR_ROW_INDEX 0x1u /* moe_finalize: a row index outside [-1, n_rows); that term was skipped */
 #define MOE_DEVERR_EXPERT_ID 0x2u /* moe_build_routing_lists: an expert id outside [0, E); that pair was dropped */
 #define MOE_DEVERR_TIMEOUT 0x4u   /* a bounded wait inside a kernel gave up; that kernel's output is invalid */
+#define MOE_DEVERR_CAPACITY 0x8u  /* moe_build_unit_windows: more units than max_units; those past it were not written */
 
 /* Weight dtypes for moe_finalize. */
 #define MOE_DTYPE_F32 0
@@ -231,6 +232,35 @@ int moe_build_routing_lists(const int32_t* ids, int T, int K, int E, int32_t* of
                             moe_stream_t stream);
 
 /* -------------------------------------------------------------------------------
+ * Unit windows: the work units a grouped expert engine takes from the routing lists,
+ * each touched expert once per `window` of its listed pairs.
+ * Source: [wide] module docstring ("unit windows built from the routing lists: every
+ * touched expert streams once per 8 of its tokens").
+ *
+ *   n_e = offsets[e+1] - offsets[e];  expert e has ceil(n_e / window) units;
+ *   unit_offsets = exclusive prefix sum of those counts (unit_offsets[E] = units);
+ *   unit u = unit_offsets[e] + j of expert e:
+ *     unit_expert[u] = e, unit_start[u] = offsets[e] + j*window,
+ *     unit_len[u] = min(window, offsets[e+1] - unit_start[u])
+ *   i.e. the list positions pairs[unit_start[u] .. unit_start[u] + unit_len[u]).
+ *
+ *   offsets      device, int32 [E + 1]   routing-list offsets (moe_build_routing_lists)
+ *   unit_offsets device, int32 [E + 1]   output
+ *   unit_expert, unit_start, unit_len    device, int32 [max_units]  outputs
+ *   max_units    their capacity; moe_unit_windows_capacity(T, K, E, window) units
+ *                always suffice for lists of T*K pairs (ceil(T*K/window) + E, at most
+ *                T*K). Units past max_units are not written and set
+ *                MOE_DEVERR_CAPACITY; unit_offsets is complete either way.
+ * Requirements: 1 <= E <= MOE_MAX_EXPERTS, window >= 1, max_units >= 0; pointers
+ * 4-byte aligned. offsets must be non-decreasing (as the lists call writes them).
+ * One launch of one CTA; deterministic, bit-exact.
+ * moe_unit_windows_capacity returns -1 for invalid sizes.
+ * ------------------------------------------------------------------------------- */
+int moe_unit_windows_capacity(int T, int K, int E, int window);
+int moe_build_unit_windows(const int32_t* offsets, int E, int window, int32_t* unit_offsets, int32_t* unit_expert,
+                           int32_t* unit_start, int32_t* unit_len, int max_units, moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
  * MXFP8 (OCP Microscaling) quantisation of BF16 rows.
  * Source: [wide] module docstring ("MXFP8 activations") and WideRoute (the token's
  * MXFP8 plan row written from its BF16 latent); [ep] module docstring ("the MXFP8
@@ -276,6 +306,31 @@ int moe_finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index,
                  const void* weights, int weights_dtype, const uint16_t* shared,
                  float routed_scaling_factor, int T, int K, int H, uint16_t* out,
                  moe_stream_t stream);
+
+/* -------------------------------------------------------------------------------
+ * Finalize with the RMSNorm epilogue: the routed latent (as moe_finalize without a
+ * shared row) and its RMS-normalised copy, in one pass over the rows.
+ * Source: [ep] EpMoeLayer.forward / stock_order (routed = the experts' weighted sum,
+ * then rms_norm(normed, routed, w["norm"], eps = 1e-5)); [wide] WideMoE.tail (the
+ * latent's RMSNorm, fused with its all-reduce; one GPU has no all-reduce).
+ *
+ *   routed[t, c] = the moe_finalize output (bit-identical; FP32 fma over k, one BF16 rounding)
+ *   x = routed[t, :] as FP32,  ss = sum_c x[c]^2 (FP32, fixed blocked order)
+ *   out[t, c] = bf16_rn( (x[c] * rsqrt_rn(ss / H + eps)) * norm_weight[c] )
+ *
+ *   rows, row_index, weights, weights_dtype, routed_scaling_factor: as moe_finalize
+ *   norm_weight device, BF16 [H]; eps >= 0 (the pages' default 1e-5)
+ *   routed      device, BF16 [T, H] output, or NULL (not written)
+ *   out         device, BF16 [T, H] output
+ * Requirements: T >= 0 (T == 0 launches nothing), 1 <= K <= MOE_MAX_TOPK, H % 256 ==
+ * 0 and 256 <= H <= 8192 (MOE_ERR_CAPACITY above); rows, out, routed and norm_weight
+ * 16-byte aligned. Row indices as moe_finalize (-1 skipped; out of range sets
+ * MOE_DEVERR_ROW_INDEX). `routed` is bit-exact; `out` is within 2^-16 relative of the
+ * exact normalisation of `routed` before its one rounding. Deterministic.
+ * ------------------------------------------------------------------------------- */
+int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, const void* weights,
+                         int weights_dtype, float routed_scaling_factor, const uint16_t* norm_weight, float eps, int T,
+                         int K, int H, uint16_t* routed, uint16_t* out, moe_stream_t stream);
 
 /* -------------------------------------------------------------------------------
  * The whole routing-and-combine step in one call.

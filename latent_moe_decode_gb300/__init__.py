@@ -19,14 +19,15 @@ from . import build as _build
 __all__ = [
     "MoeError", "load", "router_logits", "router_logits_workspace", "front_projection",
     "front_projection_workspace", "topk_route",
-    "build_routing_lists", "build_routing_lists_workspace", "mxfp8_quantize_rows",
-    "finalize", "route_finalize", "route_finalize_workspace", "device_error", "RouteFinalize",
+    "build_routing_lists", "build_routing_lists_workspace", "unit_windows", "unit_windows_capacity",
+    "mxfp8_quantize_rows",
+    "finalize", "finalize_rmsnorm", "route_finalize", "route_finalize_workspace", "device_error", "RouteFinalize",
     "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05",
-    "DEVERR_ROW_INDEX", "DEVERR_EXPERT_ID", "DEVERR_TIMEOUT",
+    "DEVERR_ROW_INDEX", "DEVERR_EXPERT_ID", "DEVERR_TIMEOUT", "DEVERR_CAPACITY",
 ]
 
 OK, ERR_INVALID_ARGUMENT, ERR_ALIGNMENT, ERR_CAPACITY, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA = range(7)
-DEVERR_ROW_INDEX, DEVERR_EXPERT_ID, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+DEVERR_ROW_INDEX, DEVERR_EXPERT_ID, DEVERR_TIMEOUT, DEVERR_CAPACITY = 0x1, 0x2, 0x4, 0x8
 ROUTER_AUTO, ROUTER_SIMT, ROUTER_TCGEN05 = 0, 1, 2
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
@@ -46,8 +47,11 @@ SIGNATURES = {
     "moe_topk_route_quantize": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "moe_build_routing_lists_workspace": (_SZ, [_I, _I, _I]),
     "moe_build_routing_lists": (_I, [_P, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "moe_unit_windows_capacity": (_I, [_I, _I, _I, _I]),
+    "moe_build_unit_windows": (_I, [_P, _I, _I, _P, _P, _P, _P, _I, _P]),
     "mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_finalize": (_I, [_P, ctypes.c_int64, _P, _P, _I, _P, _F, _I, _I, _I, _P, _P]),
+    "moe_finalize_rmsnorm": (_I, [_P, ctypes.c_int64, _P, _P, _I, _F, _P, _F, _I, _I, _I, _P, _P, _P]),
     "moe_route_finalize_workspace": (_SZ, [_I, _I, _I, _I]),
     "moe_route_finalize": (_I, [_P] * 5 + [_I] * 6 + [_F] + [_P] * 9 + [_P, _SZ, _P]),
 }
@@ -214,6 +218,38 @@ def build_routing_lists(ids, E: int, offsets=None, pairs=None, workspace=None, s
     return offsets, pairs
 
 
+def unit_windows_capacity(T: int, K: int, E: int, window: int = 8) -> int:
+    n = int(load().moe_unit_windows_capacity(T, K, E, window))
+    if n < 0:
+        raise MoeError("moe_unit_windows_capacity", ERR_INVALID_ARGUMENT)
+    return n
+
+
+def unit_windows(offsets, window: int = 8, max_units: int | None = None, unit_offsets=None, unit_expert=None,
+                 unit_start=None, unit_len=None, stream=None):
+    """Units of `window` listed pairs per expert from CSR offsets int32 [E+1]:
+    (unit_offsets [E+1], unit_expert, unit_start, unit_len [max_units]); the first
+    unit_offsets[E] entries are the units."""
+    E = offsets.shape[0] - 1
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    if max_units is None:
+        max_units = unit_expert.shape[0] if unit_expert is not None else None
+    if max_units is None:
+        raise ValueError("max_units (or preallocated unit arrays) required: see unit_windows_capacity()")
+    unit_offsets = _empty((E + 1,), torch.int32, offsets) if unit_offsets is None else _need(unit_offsets, torch.int32, (E + 1,), "unit_offsets")
+    outs = []
+    for t, name in ((unit_expert, "unit_expert"), (unit_start, "unit_start"), (unit_len, "unit_len")):
+        if t is None:
+            t = _empty((max_units,), torch.int32, offsets)
+        elif _need(t, torch.int32, None, name).dim() != 1 or t.shape[0] < max_units:
+            raise ValueError(f"{name}: expected a 1-D tensor of at least {max_units} entries")
+        outs.append(t)
+    _check("moe_build_unit_windows", load().moe_build_unit_windows(
+        _ptr(offsets), E, int(window), _ptr(unit_offsets), _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), int(max_units),
+        _stream(stream)))
+    return (unit_offsets, *outs)
+
+
 def mxfp8_quantize_rows(x, q=None, scales=None, stream=None):
     """(E4M3 bytes uint8 [rows, cols], E8M0 scale bytes uint8 [rows, cols/32])."""
     rows, cols = x.shape
@@ -245,6 +281,32 @@ def finalize(rows, weights, T: int, K: int, row_index=None, shared=None, scale: 
         _ptr(rows), n_rows, _ptr(row_index), _ptr(weights), dt, _ptr(shared), float(scale), T, K, H, _ptr(out),
         _stream(stream)))
     return out
+
+
+def finalize_rmsnorm(rows, weights, T: int, K: int, norm_weight, eps: float = 1e-5, row_index=None,
+                     scale: float = 1.0, routed=None, out=None, want_routed: bool = True, stream=None):
+    """(routed BF16 [T, H] or None, RMSNorm(routed) * norm_weight BF16 [T, H])."""
+    n_rows, H = rows.shape
+    _need(rows, torch.bfloat16, (n_rows, H), "rows")
+    if weights.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif weights.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError("weights: expected float32 or bfloat16")
+    _need(weights, weights.dtype, (T, K), "weights")
+    _need(norm_weight, torch.bfloat16, (H,), "norm_weight")
+    if row_index is not None:
+        _need(row_index, torch.int32, (T, K), "row_index")
+    if routed is None and want_routed:
+        routed = _empty((T, H), torch.bfloat16, rows)
+    elif routed is not None:
+        _need(routed, torch.bfloat16, (T, H), "routed")
+    out = _empty((T, H), torch.bfloat16, rows) if out is None else _need(out, torch.bfloat16, (T, H), "out")
+    _check("moe_finalize_rmsnorm", load().moe_finalize_rmsnorm(
+        _ptr(rows), n_rows, _ptr(row_index), _ptr(weights), dt, float(scale), _ptr(norm_weight), float(eps), T, K, H,
+        _ptr(routed), _ptr(out), _stream(stream)))
+    return routed, out
 
 
 def device_error(clear: bool = True) -> int:

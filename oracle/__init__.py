@@ -62,6 +62,9 @@ def _load():
         lib.oracle_topk_route.restype = I
         lib.oracle_routing_lists.argtypes = [P, I, I, I, P, P]
         lib.oracle_routing_lists.restype = I
+        lib.oracle_rmsnorm.argtypes = [P, P, I, I, ctypes.c_double, P]
+        lib.oracle_unit_windows.argtypes = [P, I, I, P, P, P, P, I]
+        lib.oracle_unit_windows.restype = I
         lib.oracle_mxfp8_quantize.argtypes = [P, I, I, P, P]
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -167,6 +170,20 @@ def routing_lists(ids, E):
     return off, pairs
 
 
+def unit_windows(offsets, window=8):
+    """(unit_offsets int32 [E+1], unit_expert, unit_start, unit_len int32 [units])."""
+    offsets = _c(offsets, np.int32)
+    E = offsets.size - 1
+    cap = max(1, int(offsets[-1]))
+    uo = np.empty(E + 1, np.int32)
+    ue, us, ul = (np.empty(cap, np.int32) for _ in range(3))
+    rc = _load().oracle_unit_windows(_ptr(offsets), E, int(window), _ptr(uo), _ptr(ue), _ptr(us), _ptr(ul), cap)
+    if rc != 0:
+        raise ValueError(f"oracle_unit_windows failed ({rc})")
+    n = int(uo[-1])
+    return uo, ue[:n], us[:n], ul[:n]
+
+
 def mxfp8_quantize(x):
     """E4M3 bytes [rows, cols] and E8M0 scale bytes [rows, cols/32]."""
     x = _c(x, np.uint16)
@@ -201,6 +218,22 @@ def finalize(rows, weights, T, K, row_index=None, shared=None, scale=1.0):
     if rc != 0:
         raise ValueError(f"oracle_finalize failed ({rc})")
     return out
+
+
+def rmsnorm(x, g, eps=1e-5):
+    """FP64 RMSNorm of BF16 rows x [T, H] with BF16 weight g [H]."""
+    x = _c(x, np.uint16)
+    g = _c(g, np.uint16)
+    T, H = x.shape
+    assert g.shape == (H,)
+    y = np.empty((T, H), np.float64)
+    _load().oracle_rmsnorm(_ptr(x), _ptr(g), T, H, float(eps), _ptr(y))
+    return y
+
+
+def rmsnorm_bounds(y, rel_tol=2.0 ** -16):
+    """BF16 bits (lo, hi): every value within rel_tol * |y| of y rounds into [lo, hi]."""
+    return f64_to_bf16(y - rel_tol * np.abs(y)), f64_to_bf16(y + rel_tol * np.abs(y))
 
 
 def bf16_to_f32(b: int) -> float:

@@ -304,6 +304,32 @@ int oracle_routing_lists(const int32_t* ids, int T, int K, int E, int32_t* offse
 }
 
 /* ------------------------------------------------------------------------- */
+/* Unit windows of the routing lists.
+ * [wide] module docstring: the wide grouped engine's units are "built from the
+ * routing lists: every touched expert streams once per 8 of its tokens". Read as:
+ * expert e's list is cut, in list order, into consecutive windows of `window` pairs
+ * (the last one shorter); the units are numbered expert by expert. */
+int oracle_unit_windows(const int32_t* offsets, int E, int window, int32_t* unit_offsets,
+                        int32_t* unit_expert, int32_t* unit_start, int32_t* unit_len,
+                        int max_units) {
+  int u = 0;
+  for (int e = 0; e < E; ++e) {
+    unit_offsets[e] = u;
+    for (int pos = offsets[e]; pos < offsets[e + 1]; pos += window) {
+      if (u >= max_units) return -1;
+      int len = offsets[e + 1] - pos;
+      if (len > window) len = window;
+      unit_expert[u] = e;
+      unit_start[u] = pos;
+      unit_len[u] = len;
+      ++u;
+    }
+  }
+  unit_offsets[E] = u;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* MXFP8 quantisation of BF16 rows.
  * [wide] module docstring: "MXFP8 activations"; [ep] module docstring: "the MXFP8
  * latent (bit-identical to mxfp8_quantize)"; [wide] WideRoute: the plan row of a
@@ -462,6 +488,30 @@ int oracle_finalize(const uint16_t* rows, long n_rows, const int32_t* row_index,
   return 0;
 }
 
+/* ------------------------------------------------------------------------- */
+/* RMSNorm of the routed latent (the tolerance reference).
+ * [ep] EpMoeLayer.forward / stock_order: normed = rms_norm(routed, w["norm"], eps),
+ * eps defaulting to 1e-5; [wide] WideMoE.tail: the RMSNorm of the latent. The pages
+ * give no formula beyond the name; the plainest reading is the usual one:
+ *   y[c] = x[c] / sqrt(mean_c x[c]^2 + eps) * g[c],
+ * here in FP64 from the BF16 values x (the routed latent, already rounded to BF16 by
+ * Finalize) and g. The GPU's FP32 result, rounded once to BF16, is compared against
+ * this value within a relative tolerance. */
+void oracle_rmsnorm(const uint16_t* x, const uint16_t* g, int T, int H, double eps, double* y) {
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* xr = x + (size_t)t * H;
+    double ss = 0.0;
+    for (int c = 0; c < H; ++c) {
+      const double v = (double)bf16_to_f32(xr[c]);
+      ss += v * v;
+    }
+    const double inv = 1.0 / sqrt(ss / (double)H + eps);
+    for (int c = 0; c < H; ++c)
+      y[(size_t)t * H + c] = (double)bf16_to_f32(xr[c]) * inv * (double)bf16_to_f32(g[c]);
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* BF16 helpers exposed for the tests' own checks of the conversions. */
 float oracle_bf16_to_f32(uint16_t b) { return bf16_to_f32(b); }
 uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }

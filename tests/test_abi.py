@@ -85,6 +85,25 @@ def test_validation_before_any_cuda_call(lib):
     assert chain(8, 0, A16) == 1
     assert chain(8, 16, None) == 1
     assert lib.moe_router_logits_ex(P(264), A16, A16, 8, 7168, 896, None, 0, 0, None) == 2
+    assert lib.moe_build_unit_windows(A16, 0, 8, A16, A16, A16, A16, 4, None) == 1
+    assert lib.moe_build_unit_windows(A16, 896, 0, A16, A16, A16, A16, 4, None) == 1
+    assert lib.moe_build_unit_windows(A16, 1025, 8, A16, A16, A16, A16, 4, None) == 3
+    assert lib.moe_build_unit_windows(A16, 896, 8, A16, None, A16, A16, 4, None) == 1
+    assert lib.moe_build_unit_windows(P(258), 896, 8, A16, A16, A16, A16, 4, None) == 2
+    assert lib.moe_unit_windows_capacity(1020, 16, 896, 8) == 2040 + 896
+    assert lib.moe_unit_windows_capacity(10, 16, 896, 8) == 160  # at most one unit per pair
+    assert lib.moe_unit_windows_capacity(10, 16, 896, 0) == -1
+    fn = lambda T, K, H, eps=1e-5, g=A16, wdt=1: lib.moe_finalize_rmsnorm(A16, 1 << 20, None, A16, wdt, 1.0, g, eps, T,
+                                                                           K, H, None, A16, None)
+    assert fn(-1, 16, 3584) == 1
+    assert fn(4, 0, 3584) == 1
+    assert fn(4, 16, 3500) == 1  # H % 256
+    assert fn(4, 16, 3584, eps=-1.0) == 1
+    assert fn(4, 16, 3584, wdt=2) == 1
+    assert fn(4, 16, 8448) == 3  # H > 8192
+    assert fn(4, 16, 3584, g=None) == 1
+    assert fn(4, 16, 3584, g=P(264)) == 2
+    assert fn(0, 16, 3584) == 0  # T = 0: no-op
     front = lambda T, H, E, L, x=A16, wd=A16, lat=A16: lib.moe_front_projection(x, A16, wd, A16, lat, T, H, E, L, None,
                                                                                0, None)
     assert front(0, 7168, 896, 3584) == 1

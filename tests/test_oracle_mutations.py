@@ -10,7 +10,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PINS = ["test_oracle_conversions.py", "test_oracle_router.py", "test_oracle_sigmoid.py",
-        "test_oracle_topk.py", "test_oracle_lists.py", "test_oracle_mxfp8.py", "test_oracle_finalize.py"]
+        "test_oracle_topk.py", "test_oracle_lists.py", "test_oracle_mxfp8.py", "test_oracle_finalize.py",
+        "test_oracle_front.py", "test_oracle_units.py", "test_oracle_norm.py"]
 
 MUTATIONS = {
     "router_wrong_row": ("const uint16_t* wr = w + (size_t)e * H;\n      for", "const uint16_t* wr = w + (size_t)(e ? e - 1 : 0) * H;\n      for"),
@@ -36,6 +37,13 @@ MUTATIONS = {
     "fin_shared_twice": ("if (shared) acc = acc + bf16_to_f32(shared[(size_t)t * H + c]);",
                          "if (shared) acc = acc + 2.0f * bf16_to_f32(shared[(size_t)t * H + c]);"),
     "bf16_truncate": ("  u += 0x7FFFu + lsb;", "  u += 0u * lsb;"),
+    "f64_bf16_via_f32": ("const double r = nearbyint(a / step) * step;", "const double r = (double)(float)a;"),
+    "f64_bf16_nine_bits": ("const double step = ldexp(1.0, lead - 7);", "const double step = ldexp(1.0, lead - 8);"),
+    "units_len_full": ("if (len > window) len = window;", "len = window;"),
+    "units_one_per_expert": ("pos += window) {", "pos += window + offsets[e + 1]) {"),
+    "norm_sum_not_mean": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);", "const double inv = 1.0 / sqrt(ss + eps);"),
+    "norm_eps_outside": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);", "const double inv = 1.0 / (sqrt(ss / (double)H) + eps);"),
+    "norm_no_gamma": ("* inv * (double)bf16_to_f32(g[c]);", "* inv;"),
 }
 
 
