@@ -623,6 +623,56 @@ def run_ncu_norm(args):
     torch.cuda.synchronize()
 
 
+def units_inputs(T, dev):
+    """Routing lists of the wide batch's top-16 (oracle-free: the library's own chain
+    at seed 0) for the unit-window timings."""
+    import latent_moe_decode_gb300 as m
+
+    step = Step(T, dev, graph=False)
+    step.run()
+    return step.rf.offsets.clone(), m.unit_windows_capacity(T, synth.K, synth.E, 8)
+
+
+def run_units(args):
+    """Unit windows (8 pairs per unit) from the routing lists, one JSON line per T, each
+    call timed back to back."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    stream = torch.cuda.current_stream()
+    for T in [int(t) for t in args.units.split(",")]:
+        off, cap = units_inputs(T, dev)
+        bufs = [torch.empty(cap, dtype=torch.int32, device=dev) for _ in range(3)]
+        uo = torch.empty(synth.E + 1, dtype=torch.int32, device=dev)
+        call = lambda: m.unit_windows(off, 8, max_units=cap, unit_offsets=uo, unit_expert=bufs[0], unit_start=bufs[1],
+                                      unit_len=bufs[2])
+        for _ in range(args.warmup):
+            call()
+        ms = time_back_to_back([call] * args.steps, stream)
+        n = int(uo[-1].item())
+        print(json.dumps({"T": T, "us": round(ms * 1e3, 2), "units": n, "pairs": T * synth.K,
+                          "bytes": 4 * (synth.E + 1) * 2 + 12 * n, "timing": "back to back, one call per launch"}),
+              flush=True)
+        assert m.device_error(clear=True) == 0
+
+
+def run_ncu_units(args):
+    """Unit windows at T (default 1020), untimed (for profiler captures)."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    off, cap = units_inputs(args.T or T_WIDE, dev)
+    for _ in range(args.warmup + args.steps):
+        m.unit_windows(off, 8, max_units=cap)
+    torch.cuda.synchronize()
+
+
 def run_ncu_step(args):
     """The wide step, untimed, warmup + steps times (for profiler captures)."""
     import torch
@@ -715,6 +765,8 @@ def main():
     ap.add_argument("--ncu-front", action="store_true", help="run the front projection untimed (for profiler captures)")
     ap.add_argument("--norm", default=None, help="comma-separated T list: time Finalize with the RMSNorm epilogue")
     ap.add_argument("--ncu-norm", action="store_true", help="run Finalize with the RMSNorm epilogue untimed (profiling)")
+    ap.add_argument("--units", default=None, help="comma-separated T list: time the unit windows of the routing lists")
+    ap.add_argument("--ncu-units", action="store_true", help="run the unit windows untimed (for profiler captures)")
     ap.add_argument("--T", type=int, default=0, help="with --ncu-step: token count (default 1020)")
     ap.add_argument("--router-algo", type=int, default=0, help="with --ncu-step: router kernel family")
     args = ap.parse_args()
@@ -734,6 +786,12 @@ def main():
         return
     if args.ncu_norm:
         run_ncu_norm(args)
+        return
+    if args.ncu_units:
+        run_ncu_units(args)
+        return
+    if args.units:
+        run_units(args)
         return
     if args.norm:
         run_norm(args)
