@@ -136,11 +136,12 @@ int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, float* logit
  * hidden rows in one tensor-core launch (one pass over x for both weights).
  *   logits[t, e] = sum_j x[t, j] * w_router[e, j]                 FP32 [T, E]
  *   latent[t, l] = bf16_rn( sum_j x[t, j] * w_down[l, j] )        BF16 [T, L]
- * Source: [wide] module docstring ("front one FP32-out GEMM over this rank's router
- * rows and latent down shard"; precision: "FP32 router logits, the latent rounded once
- * to BF16 (as the stock GEMM epilogue)"); [wide] WideMoE.__init__ (`packed`: the
- * router rows stacked on the latent down rows); [ep] EpMoeLayer.stock_order
- * (front = mm(x, front^T), the latent its last 3584 columns, BF16).
+ * Source: [wide] module docstring (the front is a single GEMM with FP32 output over
+ * the rank's router rows and its share of the latent down projection; precision
+ * paragraph: logits stay FP32, the latent is rounded to BF16 once, like the stock
+ * GEMM's epilogue); [wide] WideMoE.__init__ (`packed`: the router rows stacked on the
+ * latent down rows); [ep] EpMoeLayer.stock_order (front = mm(x, front^T), the latent
+ * its last 3584 columns, BF16).
  *
  *   x         device, BF16 [T, H]        hidden rows
  *   w_router  device, BF16 [E, H]        router weight (gate)
@@ -234,8 +235,8 @@ int moe_build_routing_lists(const int32_t* ids, int T, int K, int E, int32_t* of
 /* -------------------------------------------------------------------------------
  * Unit windows: the work units a grouped expert engine takes from the routing lists,
  * each touched expert once per `window` of its listed pairs.
- * Source: [wide] module docstring ("unit windows built from the routing lists: every
- * touched expert streams once per 8 of its tokens").
+ * Source: [wide] module docstring (the grouped engine's unit windows come from the
+ * routing lists; each expert with tokens is read once per 8 of them).
  *
  *   n_e = offsets[e+1] - offsets[e];  expert e has ceil(n_e / window) units;
  *   unit_offsets = exclusive prefix sum of those counts (unit_offsets[E] = units);

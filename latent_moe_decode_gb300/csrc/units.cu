@@ -2,8 +2,8 @@
 // streams each touched expert's weights once per `window` of its tokens.
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, module
-// docstring (the wide grouped engine's "unit windows built from the routing lists:
-// every touched expert streams once per 8 of its tokens").
+// docstring (the wide grouped engine takes its work units from the routing lists,
+// reading each expert that has tokens once for every 8 of them).
 //
 // For each expert e with n_e = offsets[e+1] - offsets[e] listed pairs there are
 // ceil(n_e / W) units; unit j of e covers list positions offsets[e] + jW ..

@@ -104,7 +104,7 @@ void oracle_router_logits_sampled(const uint16_t* x, const uint16_t* w, int H, i
 /* ------------------------------------------------------------------------- */
 /* Latent down projection: the front GEMM's latent columns.
  * [wide] module docstring: one front GEMM over the router rows and the latent down
- * rows, and "the latent rounded once to BF16 (as the stock GEMM epilogue)";
+ * rows, the latent then rounded to BF16 a single time, as the stock GEMM's epilogue does;
  * [ep] EpMoeLayer.stock_order: front = mm(x, front^T) in BF16.
  * The exact sum is oracle_router_logits over the down-projection rows. The one
  * rounding to BF16 is done here straight from the double (nearest, ties to even):
@@ -305,8 +305,8 @@ int oracle_routing_lists(const int32_t* ids, int T, int K, int E, int32_t* offse
 
 /* ------------------------------------------------------------------------- */
 /* Unit windows of the routing lists.
- * [wide] module docstring: the wide grouped engine's units are "built from the
- * routing lists: every touched expert streams once per 8 of its tokens". Read as:
+ * [wide] module docstring: the wide grouped engine takes its units from the
+ * routing lists, each expert that has tokens read once per 8 of them. Read as:
  * expert e's list is cut, in list order, into consecutive windows of `window` pairs
  * (the last one shorter); the units are numbered expert by expert. */
 int oracle_unit_windows(const int32_t* offsets, int E, int window, int32_t* unit_offsets,

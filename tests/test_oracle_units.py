@@ -1,6 +1,6 @@
-"""Pins of the oracle's unit windows (wide page, module docstring: every touched
-expert streams once per 8 of its tokens) by closed forms and by invariants checked
-against the routing lists they cut."""
+"""Pins of the oracle's unit windows (wide page, module docstring: the grouped
+engine reads each expert with tokens once per 8 of them) by closed forms and by
+invariants checked against the routing lists they cut."""
 import numpy as np
 import pytest
 
