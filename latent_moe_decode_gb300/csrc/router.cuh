@@ -23,10 +23,13 @@ struct TcPlan {
 inline size_t tc_workspace(const TcPlan& p, int T, int E) {
   if (p.S <= 1) return 0;
   if (!p.cluster) return (size_t)p.S * T * E * sizeof(float);
-  const size_t tiles = (size_t)((E + 127) / 128) * ((T + p.bn - 1) / p.bn);
+  size_t m_tiles = (size_t)((E + 127) / 128);
+  if (p.pair) m_tiles = (m_tiles + 1) / 2 * 2;  // pairs of 128-row tiles (the last may be padding)
+  const size_t tiles = m_tiles * ((T + p.bn - 1) / p.bn);
   return tiles * p.S * p.bn * 128 * sizeof(float);
 }
-TcPlan tc_plan(int T, int H, int E, int sm_count);
+TcPlan tc_plan(int T, int H, int E, int sm_count);         // single CTAs or CTA pairs
+TcPlan tc_plan_single(int T, int H, int E, int sm_count);  // single CTAs only
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,
                      float* part, uint32_t* err, cudaStream_t stream);
 

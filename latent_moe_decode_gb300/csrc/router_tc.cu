@@ -309,7 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my0 = chunk_first(s, nch, S), my1 = chunk_first(s + 1, nch, S);
     const size_t tile = (size_t)mt * gridDim.y + nt;  // (a pair's two CTAs: two tiles)
     float* slot = part + (tile * S + s) * (size_t)BN * kBM;
-    if (done) {
+    // a pair's padding half (rows past both weights) computes zeros no one stores: its
+    // splits skip the exchange (still meeting at the cluster barrier)
+    const bool live = mt < mt1 + (FRONT ? (L + kBM - 1) / kBM : 0);
+    if (done && live) {
 #pragma unroll 1
       for (int ch = wg; ch < nch; ch += kGroups) {
         if (ch >= my0 && ch < my1) continue;
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cluster_sync();  // every split's partial chunks are written and visible to the cluster
-    if (done) {
+    if (done && live) {
 #pragma unroll 1
       for (int ch = my0 + wg; ch < my1; ch += kGroups) {
         uint32_t v[16];
@@ -501,7 +504,55 @@ int max_pair_clusters_bn(int bn, int n_ctas) {
 
 }  // namespace
 
+namespace {
+// CTA pairs over pairs of 128-row tiles: S pairs of a tile per cluster (at most 4: the
+// portable 8 CTAs), or no split.
+TcPlan pair_plan(int T, int H, int m_tiles, int sm_count) {
+  TcPlan p;
+  p.pair = true;
+  p.bn = 256;
+  for (int b : {32, 64, 128, 256})  // (a pair's MMA takes N >= 32)
+    if (b >= T) {
+      p.bn = b;
+      break;
+    }
+  p.n_kb = (H + kBK - 1) / kBK;
+  const int pairs = (m_tiles + 1) / 2;
+  const int tiles = pairs * ((T + p.bn - 1) / p.bn);  // pair tiles
+  int s = sm_count / (2 * (tiles > 0 ? tiles : 1));
+  s = s < 1 ? 1 : s;
+  if (s > 4) s = 4;
+  if (s > p.n_kb / 2) s = p.n_kb / 2 > 0 ? p.n_kb / 2 : 1;
+  p.S = 1;
+  p.cluster = false;
+  for (int c = s; c >= 2; --c) {
+    if (max_pair_clusters_bn(p.bn, 2 * c) >= tiles) {
+      p.S = c;
+      p.cluster = true;
+      break;
+    }
+  }
+  return p;
+}
+
+int plan_ctas(const TcPlan& p, int T, int m_tiles) {
+  const int n = (T + p.bn - 1) / p.bn;
+  return p.pair ? 2 * p.S * ((m_tiles + 1) / 2) * n : p.S * m_tiles * n;
+}
+}  // namespace
+
+// Single CTAs (M = 128) or CTA pairs (M = 256): pairs stage a third less per K block
+// for the same MMA work, so they are taken for token tiles of 128 or more whenever they
+// keep at least as many SMs busy.
 TcPlan tc_plan(int T, int H, int E, int sm_count) {
+  const TcPlan single = tc_plan_single(T, H, E, sm_count);
+  if (single.bn < 128) return single;
+  const int m_tiles = (E + kBM - 1) / kBM;
+  const TcPlan pair = pair_plan(T, H, m_tiles, sm_count);
+  return plan_ctas(pair, T, m_tiles) >= plan_ctas(single, T, m_tiles) ? pair : single;
+}
+
+TcPlan tc_plan_single(int T, int H, int E, int sm_count) {
   TcPlan p;
   p.bn = 256;
   for (int b : {16, 32, 64, 128, 256})
@@ -538,20 +589,35 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
   const bool direct = p.S == 1 || p.cluster;
   float* dst = direct ? logits : part;
   int st;
-#define MOE_TC_CASE(B)                                                                                        \
-  case B:                                                                                                      \
+#define MOE_TC_CASE(B)                                                                                         \
+  case B:                                                                                                       \
     st = p.cluster ? launch_bn<B, true, false, false>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream) \
                    : launch_bn<B, false, false, false>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream); \
     break;
-  switch (p.bn) {
-    MOE_TC_CASE(16)
-    MOE_TC_CASE(32)
-    MOE_TC_CASE(64)
-    MOE_TC_CASE(128)
-    MOE_TC_CASE(256)
-    default: return MOE_ERR_INVALID_ARGUMENT;
+#define MOE_TC_PAIR_CASE(B)                                                                                    \
+  case B:                                                                                                       \
+    st = p.cluster ? launch_bn<B, true, false, true>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream) \
+                   : launch_bn<B, false, false, true>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream); \
+    break;
+  if (p.pair) {
+    if (p.S > 1 && !p.cluster) return MOE_ERR_INVALID_ARGUMENT;
+    switch (p.bn) {
+      MOE_TC_PAIR_CASE(128)
+      MOE_TC_PAIR_CASE(256)
+      default: return MOE_ERR_INVALID_ARGUMENT;
+    }
+  } else {
+    switch (p.bn) {
+      MOE_TC_CASE(16)
+      MOE_TC_CASE(32)
+      MOE_TC_CASE(64)
+      MOE_TC_CASE(128)
+      MOE_TC_CASE(256)
+      default: return MOE_ERR_INVALID_ARGUMENT;
+    }
   }
 #undef MOE_TC_CASE
+#undef MOE_TC_PAIR_CASE
   if (st != MOE_OK || direct) return st;
   return launch_router_reduce(part, p.S, T, E, logits, stream);
 }
@@ -560,31 +626,7 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
 // one sequence: a pair may hold the last router tile and the first latent tile). Its
 // splits are reduced only on chip: a cluster of S pairs, or no split.
 TcPlan front_plan(int T, int H, int E, int L, int sm_count) {
-  TcPlan p;
-  p.pair = true;
-  p.bn = 256;
-  for (int b : {32, 64, 128, 256})  // (a pair's MMA takes N >= 32)
-    if (b >= T) {
-      p.bn = b;
-      break;
-    }
-  p.n_kb = (H + kBK - 1) / kBK;
-  const int pairs = ((E + kBM - 1) / kBM + (L + kBM - 1) / kBM + 1) / 2;
-  const int tiles = pairs * ((T + p.bn - 1) / p.bn);  // pair tiles
-  int s = sm_count / (2 * (tiles > 0 ? tiles : 1));
-  s = s < 1 ? 1 : s;
-  if (s > 4) s = 4;  // a cluster of S pairs stays within the portable 8 CTAs
-  if (s > p.n_kb / 2) s = p.n_kb / 2 > 0 ? p.n_kb / 2 : 1;
-  p.S = 1;
-  p.cluster = false;
-  for (int c = s; c >= 2; --c) {
-    if (max_pair_clusters_bn(p.bn, 2 * c) >= tiles) {
-      p.S = c;
-      p.cluster = true;
-      break;
-    }
-  }
-  return p;
+  return pair_plan(T, H, (E + kBM - 1) / kBM + (L + kBM - 1) / kBM, sm_count);
 }
 
 size_t front_workspace(const TcPlan& p, int T, int E, int L) {
