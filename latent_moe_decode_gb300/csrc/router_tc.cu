@@ -21,17 +21,18 @@
 //     chunks) and store FP32 rows; lanes hold consecutive experts, so every store
 //     instruction writes 128 contiguous bytes. The epilogue is latency-bound, hence the
 //     many warps although the mainloop needs two threads.
-// Split-K: when the S split CTAs of a tile fit as one thread-block cluster (S <= 8,
-// all co-resident), the reduction happens in the same kernel: the tile's token columns
-// are cut into 16-column chunks shared out among the S CTAs; after the mainloops each
-// CTA writes the chunks other splits own from TMEM to the caller's workspace (128
+// Split-K: when the S split CTAs of a tile fit as one thread-block cluster (S <= 8 for
+// wide token tiles; up to a non-portable 16 for tiles of 64 tokens or fewer, so that
+// more SMs stream the gate; all clusters co-resident), the reduction happens in the
+// same kernel: the CTAs write partials from TMEM to the caller's workspace (128
 // contiguous bytes per warp store, L2-resident), a cluster barrier orders those writes
-// before the reads, and each owner sums its chunks over the S partials in split order
-// (its own straight from TMEM), writes final logits (lanes = consecutive experts: 128
-// contiguous bytes per store) and invalidates the workspace lines it read in L2
-// (discard.global.L2), so the scratch never costs an HBM write-back. Otherwise (more
-// splits) the partials [S][T][E] go to the workspace and a second kernel sums them in
-// split order.
+// before the reads, and the tile's outputs are summed over the S partials in split
+// order -- wide tiles by owners of 16-column x 32-row units (their own partial
+// straight from TMEM), narrow tiles column by column over all the cluster's warps --
+// written as final logits (lanes = consecutive experts: 128 contiguous bytes per
+// store), and the workspace lines read are invalidated in L2 (discard.global.L2), so
+// the scratch never costs an HBM write-back. Otherwise the partials [S][T][E] go to
+// the workspace and a second kernel sums them in split order.
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel sets
 // MOE_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies in flight,
 // frees its TMEM and exits.
@@ -47,6 +48,7 @@ constexpr int kBM = 128;              // experts per CTA (TMEM lanes)
 constexpr int kBK = 64;               // K elements per stage (128 bytes: one swizzle span)
 constexpr int kThreads = 512;         // 16 warps: two lanes run the mainloop, all sixteen the epilogue
 constexpr int kGroups = kThreads / 128;  // warpgroups: each reaches all 128 TMEM lanes
+constexpr int kMaxSplits = 16;           // splits of a cluster plan (16: a non-portable cluster)
 
 // PAIR: two CTAs (one SM each) run one M = 256 MMA (cta_group::2); each stages its
 // own 128 weight rows and half of the BN token rows.
@@ -147,9 +149,10 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The BN token columns of a tile are cut into 16-column chunks; split r of S owns the
-// chunks [first(r), first(r + 1)).
-__host__ __device__ constexpr int chunk_first(int r, int nch, int S) { return (r * nch) / S; }
+// The reduction's units are the (16-column chunk, 32-row quarter) blocks of a tile,
+// numbered 4 * chunk + quarter; split r of S owns the units [first(r), first(r + 1)).
+// (A quarter is what one warp reads from TMEM.)
+__host__ __device__ constexpr int unit_first(int r, int units, int S) { return (r * units) / S; }
 
 // Output of one logit (or latent) value: expert tiles (mt < mt1) store FP32 logits
 // [T, E]; with FRONT, the tiles past them are rows of the second weight and store the
@@ -297,25 +300,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's 32 TMEM lanes
   const int row = (warp & 3) * 32 + lane;                           // = expert row within the tile
   if constexpr (CLUSTER) {
-    // Split s owns the 16-column chunks [first(s), first(s + 1)) of the tile. It writes
-    // the chunks other splits own from TMEM to its slot of the workspace ([column][128
-    // rows] FP32: every store instruction of a warp writes 128 contiguous bytes; 18 MB
-    // at T = 1020, resident in L2). After a cluster barrier (release / acquire at cluster
-    // scope) each owner reads its chunks of the other S - 1 partials, all loads of a
-    // split at once, sums them per column in split order with its own partial (read
-    // from TMEM) and writes the logits; it then invalidates the workspace lines it read
-    // in L2 (discard.global.L2), so the scratch is never written back to HBM.
+    // Wide tiles: split s owns the units [first(s), first(s + 1)) of the tile (16
+    // columns x 32 rows each). Every warp writes the units of its rows that other splits
+    // own from TMEM to its slot of the workspace ([column][128 rows] FP32: every store
+    // instruction of a warp writes 128 contiguous bytes; 18 MB at T = 1020, resident in
+    // L2). After a cluster barrier (release / acquire at cluster scope) each owner warp
+    // reads its units of the other S - 1 partials (a split's 16 loads at once), sums
+    // them per column in split order with its own partial (read from TMEM) and writes
+    // the logits; it then invalidates the workspace lines it read in L2
+    // (discard.global.L2), so the scratch is never written back to HBM. (Measured
+    // slower: every split's loads in flight at once, and row-contiguous 16-byte slots,
+    // which touch twice the L2 sectors.) Narrow tiles reduce by columns (below).
     constexpr int nch = BN / 16;
-    const int my0 = chunk_first(s, nch, S), my1 = chunk_first(s + 1, nch, S);
+    const int q4 = warp & 3;  // this warp's 32-row quarter
+    const int my0 = unit_first(s, 4 * nch, S), my1 = unit_first(s + 1, 4 * nch, S);
+    auto mine = [&](int ch) { return 4 * ch + q4 >= my0 && 4 * ch + q4 < my1; };
     const size_t tile = (size_t)mt * gridDim.y + nt;  // (a pair's two CTAs: two tiles)
     float* slot = part + (tile * S + s) * (size_t)BN * kBM;
     // a pair's padding half (rows past both weights) computes zeros no one stores: its
     // splits skip the exchange (still meeting at the cluster barrier)
     const bool live = mt < mt1 + (FRONT ? (L + kBM - 1) / kBM : 0);
+    if constexpr (BN <= 64) {
+      // Narrow tiles (few columns, many splits): every split writes its whole partial;
+      // after the cluster barrier each (column, 32-row quarter) of the tile is one item,
+      // dealt to the cluster's warps in turn, whose lanes load that column's S values
+      // (all in flight: one round trip), sum them in split order and store.
+      if (done && live) {
+#pragma unroll 1
+        for (int ch = wg; ch < nch; ch += kGroups) {
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)(16 * ch), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) __stcg(slot + (size_t)(16 * ch + j) * kBM + row, __uint_as_float(v[j]));
+        }
+      }
+      cluster_sync();  // every split's partial is written and visible to the cluster
+      if (done && live) {
+        const int nwarps = S * (kThreads / 32);
+#pragma unroll 1
+        for (int it = s * (kThreads / 32) + warp; it < 4 * BN; it += nwarps) {
+          const int c = it >> 2, r = (it & 3) * 32 + lane;  // column, row
+          const float* src = part + (tile * S * BN + c) * (size_t)kBM + r;  // split 0
+          float pv[kMaxSplits];
+#pragma unroll
+          for (int q = 0; q < kMaxSplits; ++q)
+            if (q < S) pv[q] = __ldcg(src + (size_t)q * BN * kBM);
+          float acc = pv[0];
+#pragma unroll
+          for (int q = 1; q < kMaxSplits; ++q)  // split order
+            if (q < S) acc = __fadd_rn(acc, pv[q]);
+          __syncwarp();  // every lane's loads are consumed before their lines are invalidated
+          if (discard && lane < S)  // split `lane`'s line of this column and quarter
+            asm volatile("discard.global.L2 [%0], 128;" ::"l"(src - r + (it & 3) * 32 + (size_t)lane * BN * kBM)
+                         : "memory");
+          const int t = nt * BN + c;
+          if (t < T) store_out<FRONT>(out, out2, t, mt, mt1, r, E, L, acc);
+        }
+      }
+    } else {
     if (done && live) {
 #pragma unroll 1
       for (int ch = wg; ch < nch; ch += kGroups) {
-        if (ch >= my0 && ch < my1) continue;
+        if (mine(ch)) continue;
         uint32_t v[16];
         tmem_ld16(tl + (uint32_t)(16 * ch), v);
         tmem_wait_ld();
@@ -326,13 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();  // every split's partial chunks are written and visible to the cluster
     if (done && live) {
 #pragma unroll 1
-      for (int ch = my0 + wg; ch < my1; ch += kGroups) {
+      for (int ch = my0 / 4 + wg; ch < (my1 + 3) / 4; ch += kGroups) {
+        if (!mine(ch)) continue;  // (warp-uniform)
         uint32_t v[16];
         tmem_ld16(tl + (uint32_t)(16 * ch), v);
         tmem_wait_ld();
         float acc[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // split order; each split's 16 columns loaded at once
+        for (int q = 0; q < 8; ++q) {  // split order (S <= 8 here); a split's 16 columns loaded at once
           if (q >= S) break;
           float p[16];
           if (q == s) {
@@ -361,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    }  // BN > 64
   } else if (done) {
     float* dst = out + (size_t)s * T * E;  // (FRONT plans have S == 1)
 #pragma unroll 1
@@ -443,6 +492,9 @@ int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* d
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (CLUSTER || PAIR) ? 1 : 0;
+  if (attr[0].val.clusterDim.x > 8 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return MOE_ERR_CUDA;
   const int discard = (reinterpret_cast<uintptr_t>(part) & 127u) == 0 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_w2, dst, out2, part, T, E, L, mt1, p.n_kb, p.S, discard, err) ==
                  cudaSuccess
@@ -454,12 +506,13 @@ int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* d
 // at once.
 template <int BN, bool PAIR = false>
 int max_clusters(int S) {
-  static int cache[9] = {0};
-  if (S < 2 || S > 8) return 0;
+  static int cache[kMaxSplits + 1] = {0};
+  if (S < 2 || S > kMaxSplits) return 0;
   if (cache[S]) return cache[S];
   auto kern = router_tc_kernel<BN, true, false, PAIR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN, PAIR>::kSmem) !=
-      cudaSuccess) {
+          cudaSuccess ||
+      (S > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
     cudaGetLastError();
     return 0;
   }
@@ -566,12 +619,15 @@ TcPlan tc_plan_single(int T, int H, int E, int sm_count) {
   s = s < 1 ? 1 : s;
   s = s > 32 ? 32 : s;
   if (s > p.n_kb / 2) s = p.n_kb / 2 > 0 ? p.n_kb / 2 : 1;
-  // at most one portable cluster of splits: at small T the on-chip reduction in one
-  // kernel beats more splits reduced through a workspace by a second kernel
-  if (s > 8) s = 8;
+  // at most one cluster of splits: the on-chip reduction in one kernel beats more
+  // splits reduced through a workspace by a second kernel. Narrow token tiles (BN <= 64,
+  // a few tiles) go up to a non-portable cluster of 16 so that more SMs stream the
+  // weight; wider tiles stay within the portable 8 (their exchange grows with S).
+  const int cap = p.bn <= 64 ? kMaxSplits : 8;
+  if (s > cap) s = cap;
   p.S = s;
   p.cluster = false;
-  if (s >= 2 && s <= 8) {
+  if (s >= 2) {
     // the largest cluster of splits whose clusters are all resident at once
     for (int c = s; c >= 2; --c) {
       if (max_clusters_bn(p.bn, c) >= tiles) {
