@@ -605,14 +605,11 @@ TcPlan tc_plan(int T, int H, int E, int sm_count) {
   return plan_ctas(pair, T, m_tiles) >= plan_ctas(single, T, m_tiles) ? pair : single;
 }
 
-TcPlan tc_plan_single(int T, int H, int E, int sm_count) {
+namespace {
+// The split-K plan for one token tile width bn.
+TcPlan plan_for_bn(int bn, int T, int H, int E, int sm_count) {
   TcPlan p;
-  p.bn = 256;
-  for (int b : {16, 32, 64, 128, 256})
-    if (b >= T) {
-      p.bn = b;
-      break;
-    }
+  p.bn = bn;
   p.n_kb = (H + kBK - 1) / kBK;
   const int tiles = ((E + kBM - 1) / kBM) * ((T + p.bn - 1) / p.bn);
   int s = sm_count / (tiles > 0 ? tiles : 1);
@@ -638,6 +635,27 @@ TcPlan tc_plan_single(int T, int H, int E, int sm_count) {
     }
   }
   return p;
+}
+}  // namespace
+
+// The token tile is the narrowest of 16 .. 256 that covers T; when its plan would keep
+// fewer than 70 % of the SMs busy (few tiles, splits capped), narrower tiles are tried
+// (more tiles, each with less to exchange), down to 64 columns.
+TcPlan tc_plan_single(int T, int H, int E, int sm_count) {
+  int bn = 256;
+  for (int b : {16, 32, 64, 128, 256})
+    if (b >= T) {
+      bn = b;
+      break;
+    }
+  const int m_tiles = (E + kBM - 1) / kBM;
+  auto ctas = [&](const TcPlan& q) { return q.S * m_tiles * ((T + q.bn - 1) / q.bn); };
+  TcPlan best = plan_for_bn(bn, T, H, E, sm_count);
+  for (int b = bn / 2; b >= 64 && 10 * ctas(best) < 7 * sm_count; b /= 2) {
+    const TcPlan q = plan_for_bn(b, T, H, E, sm_count);
+    if (ctas(q) > ctas(best)) best = q;
+  }
+  return best;
 }
 
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,
