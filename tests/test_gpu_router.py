@@ -20,7 +20,10 @@ def _ints(seed, shape, lo=-8, hi=8):
 
 @pytest.mark.parametrize("algo", list(ALGOS))
 @pytest.mark.parametrize("T,E,H", [(1, 896, 7168), (8, 896, 7168), (17, 128, 1024), (64, 896, 7168), (100, 200, 512),
-                                   (300, 896, 1024), (1020, 256, 7168)])
+                                   (300, 896, 1024), (1020, 256, 7168),
+                                   # plan branches at the full gate: 64-column tiles (T = 128), 128-column
+                                   # tiles (T = 256); CTA pairs with a padding half and a split (T = 2048)
+                                   (128, 896, 7168), (256, 896, 7168), (2048, 896, 1024)])
 def test_integer_exact(moe, orc, algo, T, E, H):
     x, w = _ints(T, (T, H)), _ints(E + 1, (E, H))
     got = host(moe.router_logits(bf16_dev(x), bf16_dev(w), algo=ALGOS[algo]))
@@ -39,7 +42,7 @@ def test_random_within_tolerance(moe, orc, algo, T, E, H):
 
 
 @pytest.mark.parametrize("algo", list(ALGOS))
-@pytest.mark.parametrize("T", [1020, 4096])
+@pytest.mark.parametrize("T", [1020, 2048, 4096])
 def test_full_size_sampled(moe, orc, algo, T):
     """The full decode shapes (896 x 7168 gate): 3000 sampled outputs against FP64."""
     x = synth.hidden_rows(T)
