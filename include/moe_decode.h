@@ -280,6 +280,21 @@ int moe_build_unit_windows(const int32_t* offsets, int E, int window, int32_t* u
 int mxfp8_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
                         moe_stream_t stream);
 
+/* The same with a choice of the scale rule:
+ *   MXFP8_SCALE_FLOOR (what mxfp8_quantize_rows does): se = floor(log2 amax) - 8, the
+ *     OCP rule; elements above 448 * 2^se saturate to +-448.
+ *   MXFP8_SCALE_CEIL: se = ceil(log2(amax / 448)), the smallest power of two with
+ *     amax / 2^se <= 448, so no element saturates (one step above the OCP scale when
+ *     the block maximum's significand exceeds 1.75, the same scale otherwise).
+ * Source: [ep] module docstring (the latent's MXFP8 bit-identical to the stock
+ * mxfp8_quantize, whose scale rule the pages do not show: both readings are offered).
+ * Clamping, special blocks, layouts and requirements as mxfp8_quantize_rows; another
+ * rule returns MOE_ERR_INVALID_ARGUMENT. */
+#define MXFP8_SCALE_FLOOR 0
+#define MXFP8_SCALE_CEIL 1
+int mxfp8_quantize_rows_ex(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales, int scale_rule,
+                           moe_stream_t stream);
+
 /* -------------------------------------------------------------------------------
  * Finalize: the routing-weighted top-K sum, optionally with the shared expert.
  * Source: [wide] Finalize (out[t] = sum_k w[t,k] * rows[16t + k], FP32, k in order,

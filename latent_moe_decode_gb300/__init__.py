@@ -22,13 +22,14 @@ __all__ = [
     "build_routing_lists", "build_routing_lists_workspace", "unit_windows", "unit_windows_capacity",
     "mxfp8_quantize_rows",
     "finalize", "finalize_rmsnorm", "route_finalize", "route_finalize_workspace", "device_error", "RouteFinalize",
-    "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05",
+    "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05", "MXFP8_SCALE_FLOOR", "MXFP8_SCALE_CEIL",
     "DEVERR_ROW_INDEX", "DEVERR_EXPERT_ID", "DEVERR_TIMEOUT", "DEVERR_CAPACITY",
 ]
 
 OK, ERR_INVALID_ARGUMENT, ERR_ALIGNMENT, ERR_CAPACITY, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA = range(7)
 DEVERR_ROW_INDEX, DEVERR_EXPERT_ID, DEVERR_TIMEOUT, DEVERR_CAPACITY = 0x1, 0x2, 0x4, 0x8
 ROUTER_AUTO, ROUTER_SIMT, ROUTER_TCGEN05 = 0, 1, 2
+MXFP8_SCALE_FLOOR, MXFP8_SCALE_CEIL = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 # Every symbol the header declares, with its ctypes signature.
@@ -50,6 +51,7 @@ SIGNATURES = {
     "moe_unit_windows_capacity": (_I, [_I, _I, _I, _I]),
     "moe_build_unit_windows": (_I, [_P, _I, _I, _P, _P, _P, _P, _I, _P]),
     "mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
+    "mxfp8_quantize_rows_ex": (_I, [_P, _I, _I, _P, _P, _I, _P]),
     "moe_finalize": (_I, [_P, ctypes.c_int64, _P, _P, _I, _P, _F, _I, _I, _I, _P, _P]),
     "moe_finalize_rmsnorm": (_I, [_P, ctypes.c_int64, _P, _P, _I, _F, _P, _F, _I, _I, _I, _P, _P, _P]),
     "moe_route_finalize_workspace": (_SZ, [_I, _I, _I, _I]),
@@ -250,14 +252,16 @@ def unit_windows(offsets, window: int = 8, max_units: int | None = None, unit_of
     return (unit_offsets, *outs)
 
 
-def mxfp8_quantize_rows(x, q=None, scales=None, stream=None):
-    """(E4M3 bytes uint8 [rows, cols], E8M0 scale bytes uint8 [rows, cols/32])."""
+def mxfp8_quantize_rows(x, q=None, scales=None, stream=None, scale_rule: int = MXFP8_SCALE_FLOOR):
+    """(E4M3 bytes uint8 [rows, cols], E8M0 scale bytes uint8 [rows, cols/32]);
+    scale_rule MXFP8_SCALE_FLOOR (OCP) or MXFP8_SCALE_CEIL (no saturation)."""
     rows, cols = x.shape
     _need(x, torch.bfloat16, (rows, cols), "x")
     q = _empty((rows, cols), torch.uint8, x) if q is None else _need(q, torch.uint8, (rows, cols), "q")
     nb = cols // 32
     scales = _empty((rows, nb), torch.uint8, x) if scales is None else _need(scales, torch.uint8, (rows, nb), "scales")
-    _check("mxfp8_quantize_rows", load().mxfp8_quantize_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scales), _stream(stream)))
+    _check("mxfp8_quantize_rows_ex", load().mxfp8_quantize_rows_ex(_ptr(x), rows, cols, _ptr(q), _ptr(scales),
+                                                                   int(scale_rule), _stream(stream)))
     return q, scales
 
 

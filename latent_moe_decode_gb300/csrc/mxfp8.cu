@@ -27,20 +27,22 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+template <bool CEIL>
 __global__ void __launch_bounds__(kThreads) mxfp8_kernel(const uint16_t* __restrict__ x, long long nchunks,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
                                                          uint32_t* err) {
-  mxfp8_impl::mxfp8_block<kThreads, kUnroll>(x, nchunks, q, scales, err, blockIdx.x);
+  mxfp8_impl::mxfp8_block<kThreads, kUnroll, CEIL>(x, nchunks, q, scales, err, blockIdx.x);
 }
 
 }  // namespace
 }  // namespace moe
 
 
-extern "C" int mxfp8_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
-                                   moe_stream_t stream) {
+extern "C" int mxfp8_quantize_rows_ex(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
+                                      int scale_rule, moe_stream_t stream) {
   using namespace moe;
   if (rows < 0 || cols < 32 || cols % 32 != 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (scale_rule != MXFP8_SCALE_FLOOR && scale_rule != MXFP8_SCALE_CEIL) return MOE_ERR_INVALID_ARGUMENT;
   if (rows == 0) return MOE_OK;
   if (!x || !q || !scales) return MOE_ERR_INVALID_ARGUMENT;
   if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 8)) return MOE_ERR_ALIGNMENT;
@@ -51,6 +53,12 @@ extern "C" int mxfp8_quantize_rows(const uint16_t* x, int rows, int cols, uint8_
   const long long per = (long long)kThreads * kUnroll;
   const long long blocks = (nchunks + per - 1) / per;
   if (blocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
-  return launch_pdl(mxfp8_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, as_cuda(stream), x, nchunks, q, scales,
+  auto kern = scale_rule == MXFP8_SCALE_CEIL ? mxfp8_kernel<true> : mxfp8_kernel<false>;
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, as_cuda(stream), x, nchunks, q, scales,
                     dev.error_word);
+}
+
+extern "C" int mxfp8_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
+                                   moe_stream_t stream) {
+  return mxfp8_quantize_rows_ex(x, rows, cols, q, scales, MXFP8_SCALE_FLOOR, stream);
 }

@@ -17,8 +17,9 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 // One CTA's 16-byte chunks [block * THREADS * UNROLL, ...) of the flat input. With
 // wait = false the CTA does not wait for the preceding kernel (the caller knows the
-// input was complete before that kernel started).
-template <int THREADS, int UNROLL>
+// input was complete before that kernel started). CEIL: the round-up scale rule (the
+// smallest power of two X with amax / X <= 448) instead of the OCP floor rule.
+template <int THREADS, int UNROLL, bool CEIL = false>
 __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long long nchunks, uint8_t* __restrict__ q,
                                             uint8_t* __restrict__ scales, uint32_t* err, long long block,
                                             bool wait = true) {
@@ -64,7 +65,13 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
       if (m != 0u) {
         const int ex = (int)(m >> 7);
         const int fl = ex ? ex - 127 : (31 - __clz((int)(m & 0x7Fu))) - 133;
-        se = min(max(fl - 8, -127), 127);
+        int up = 0;  // amax / 2^fl > 1.75 (448 = 1.75 * 2^8): one step up keeps amax / X <= 448
+        if (CEIL) {
+          const uint32_t man = ex ? (m & 0x7Fu) | 0x80u : (m & 0x7Fu);  // amax = man * 2^(fl - msb)
+          const int msb = ex ? 7 : 31 - __clz((int)man);
+          up = 4u * man > (7u << msb) ? 1 : 0;
+        }
+        se = min(max(fl - 8 + up, -127), 127);
       }
       sbyte = (uint32_t)(se + 127);
       const float mult = __int_as_float((127 - se) << 23);  // 2^-se, a normal FP32

@@ -66,6 +66,7 @@ def _load():
         lib.oracle_unit_windows.argtypes = [P, I, I, P, P, P, P, I]
         lib.oracle_unit_windows.restype = I
         lib.oracle_mxfp8_quantize.argtypes = [P, I, I, P, P]
+        lib.oracle_mxfp8_quantize_rule.argtypes = [P, I, I, I, P, P]
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -184,14 +185,18 @@ def unit_windows(offsets, window=8):
     return uo, ue[:n], us[:n], ul[:n]
 
 
-def mxfp8_quantize(x):
-    """E4M3 bytes [rows, cols] and E8M0 scale bytes [rows, cols/32]."""
+def mxfp8_quantize(x, rule=0):
+    """E4M3 bytes [rows, cols] and E8M0 scale bytes [rows, cols/32]; rule 0 = the OCP
+    floor scale, 1 = the round-up scale (no saturation)."""
     x = _c(x, np.uint16)
     rows, cols = x.shape
     assert cols % 32 == 0
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // 32), np.uint8)
-    _load().oracle_mxfp8_quantize(_ptr(x), rows, cols, _ptr(q), _ptr(s))
+    if rule == 0:
+        _load().oracle_mxfp8_quantize(_ptr(x), rows, cols, _ptr(q), _ptr(s))
+    else:
+        _load().oracle_mxfp8_quantize_rule(_ptr(x), rows, cols, int(rule), _ptr(q), _ptr(s))
     return q, s
 
 

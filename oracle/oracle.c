@@ -385,8 +385,13 @@ uint8_t oracle_e4m3_encode(double y) {
   return sign | (uint8_t)code;
 }
 
-void oracle_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q,
-                           uint8_t* scales) {
+/* rule 0: the OCP floor rule above. rule 1: the round-up rule, X = the smallest power
+ * of two with amax / X <= 448 (no element saturates): the floor exponent, plus one when
+ * amax exceeds 448 times the floor scale (a block maximum whose significand is above
+ * 1.75). The pages show neither; the ep page only says the stock quantiser's output is
+ * matched bit for bit, so both readings are kept. */
+void oracle_mxfp8_quantize_rule(const uint16_t* x, int rows, int cols, int rule, uint8_t* q,
+                                uint8_t* scales) {
   int blocks = cols / 32;
   for (int r = 0; r < rows; ++r) {
     for (int b = 0; b < blocks; ++b) {
@@ -416,6 +421,7 @@ void oracle_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q,
         continue;
       }
       int se = bf16_floor_log2(amax_bits) - 8;
+      if (rule == 1 && (double)amax > ldexp(448.0, se)) se += 1;
       if (se < -127) se = -127;
       if (se > 127) se = 127;
       *so = (uint8_t)(se + 127);
@@ -425,6 +431,11 @@ void oracle_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q,
       }
     }
   }
+}
+
+void oracle_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q,
+                           uint8_t* scales) {
+  oracle_mxfp8_quantize_rule(x, rows, cols, 0, q, scales);
 }
 
 /* E4M3 byte -> value (NaN for 0x7F/0xFF). */

@@ -73,6 +73,8 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.mxfp8_quantize_rows(A16, 4, 33, A16, A16, None) == 1
     assert lib.mxfp8_quantize_rows(A16, 4, 0, A16, A16, None) == 1
     assert lib.mxfp8_quantize_rows(P(264), 4, 64, A16, A16, None) == 2
+    assert lib.mxfp8_quantize_rows_ex(A16, 4, 64, A16, A16, 2, None) == 1
+    assert lib.mxfp8_quantize_rows_ex(A16, 4, 33, A16, A16, 1, None) == 1
     assert lib.moe_build_routing_lists(A16, 4, 0, 896, A16, A16, None, 0, None) == 1
     assert lib.moe_build_routing_lists(A16, 4, 16, 1025, A16, A16, None, 0, None) == 3
     assert lib.moe_router_logits_ex(A16, A16, A16, 0, 7168, 896, None, 0, 0, None) == 1

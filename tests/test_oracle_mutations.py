@@ -44,6 +44,9 @@ MUTATIONS = {
     "norm_sum_not_mean": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);", "const double inv = 1.0 / sqrt(ss + eps);"),
     "norm_eps_outside": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);", "const double inv = 1.0 / (sqrt(ss / (double)H) + eps);"),
     "norm_no_gamma": ("* inv * (double)bf16_to_f32(g[c]);", "* inv;"),
+    "mx_ceil_always_up": ("if (rule == 1 && (double)amax > ldexp(448.0, se)) se += 1;", "if (rule == 1) se += 1;"),
+    "mx_ceil_at_448": ("if (rule == 1 && (double)amax > ldexp(448.0, se)) se += 1;",
+                       "if (rule == 1 && (double)amax >= ldexp(448.0, se)) se += 1;"),
 }
 
 

@@ -103,3 +103,57 @@ def test_nan_inf_blocks(orc):
     q, s = orc.mxfp8_quantize(x)
     assert s.tolist() == [[0xFF, 0xFF]]
     assert np.all(q == 0x7F)
+
+
+# --- the round-up scale rule (rule 1): the smallest power of two X with amax / X <= 448
+
+
+def test_ceil_rule_closed_forms(orc):
+    # amax 448: the OCP scale already fits (1.75 * 2^8), scale byte 127, code 0x7E;
+    # amax 450 (significand above 1.75): one step up, 450 / 2 = 225 -> E4M3 224 = 0x76;
+    # amax -480: -240 = 0xF7; the floor rule saturates both to 448 (0x7E / 0xFE)
+    x = synth.f32_to_bf16_bits(np.array([[448.0] + [0.5] * 31, [450.0] + [1.0] * 31, [-480.0] + [3.0] * 31],
+                                        np.float32))
+    q, s = orc.mxfp8_quantize(x, rule=1)
+    assert s.ravel().tolist() == [127, 128, 128]
+    assert q[:, 0].tolist() == [0x7E, 0x76, 0xF7]
+    q0, s0 = orc.mxfp8_quantize(x, rule=0)
+    assert s0.ravel().tolist() == [127, 127, 127] and q0[:, 0].tolist() == [0x7E, 0x7E, 0xFE]
+
+
+@pytest.mark.parametrize("amax_bits", [0x3F80, 0x3FE0, 0x3FE1, 0x43E0, 0x43E1, 0x7F7F, 0x0080, 0x0001, 0x0007])
+def test_ceil_rule_exhaustive_against_bruteforce(orc, amax_bits):
+    """As the floor-rule check, with the scale from the definition: the smallest integer
+    k with 448 * 2^k >= amax (exact in float64), then clamped; every element is the
+    nearest E4M3 code of v / 2^k and none saturates."""
+    allb = _all_finite_bf16()
+    amax = float(synth.bf16_bits_to_f32(np.array([amax_bits], np.uint16))[0])
+    vals = allb[np.abs(synth.bf16_bits_to_f32(allb)) <= amax]
+    nblk = -(-vals.size // 31)
+    body = np.resize(vals, nblk * 31).reshape(nblk, 31)
+    x = np.concatenate([np.full((nblk, 1), amax_bits, np.uint16), body], axis=1).reshape(1, -1)
+    q, s = orc.mxfp8_quantize(x, rule=1)
+    k = -200
+    while 448.0 * 2.0 ** k < amax:
+        k += 1
+    se = min(max(k, -127), 127)
+    assert np.all(s == se + 127)
+    y = synth.bf16_bits_to_f32(x.reshape(-1)).astype(np.float64) * 2.0 ** (-se)
+    assert np.all(np.abs(y) <= 448.0)
+    np.testing.assert_array_equal(q.reshape(-1), e4m3_bruteforce(y))
+
+
+def test_ceil_rule_matches_floor_below_1_75(orc):
+    # block maxima whose significand is at most 1.75 give the same scale and codes
+    rng = np.random.default_rng(9)
+    f = (rng.uniform(-1, 1, (32, 32)) * np.exp2(rng.integers(-30, 30, (32, 1)))).astype(np.float32)
+    f[:, 0] = (np.where(np.arange(32) % 2, 1.75, 1.0 + rng.uniform(0, 0.75, 32)) * np.exp2(rng.integers(-30, 30, 32))).astype(np.float32)
+    x = synth.f32_to_bf16_bits(f)
+    amax_sig = np.abs(synth.bf16_bits_to_f32(x)).max(axis=1)
+    amax_sig = amax_sig / np.exp2(np.floor(np.log2(amax_sig)))
+    keep = amax_sig <= 1.75
+    q0, s0 = orc.mxfp8_quantize(x, rule=0)
+    q1, s1 = orc.mxfp8_quantize(x, rule=1)
+    assert keep.sum() >= 16
+    np.testing.assert_array_equal(s1[keep], s0[keep])
+    np.testing.assert_array_equal(q1[keep], q0[keep])
