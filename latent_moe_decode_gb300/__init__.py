@@ -387,7 +387,11 @@ class RouteFinalize:
 
     def _count_launches(self) -> int:
         """Kernels one run() launches."""
-        # router (+ its split-K reduce when it needs scratch), top-k + MXFP8, lists, Finalize
+        if self.router_algo == ROUTER_AUTO:
+            # the one-call step: router (its split-K partials summed by the top-K launch),
+            # top-k + MXFP8, lists, Finalize
+            return 4
+        # the four calls; a forced router family may add its split-K reduce kernel
         return 4 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0)
 
     def run(self, x, w, bias, latent, rows, stream=None):

@@ -7,10 +7,21 @@
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideMoE.run
 // (router -> route -> Finalize on one stream) and ...moe.ep.layer, EpMoeLayer.__call__.
-#include "common.cuh"
+#include "router.cuh"
+
+namespace {
+// the router's partials [S][T][E] (or its cluster workspace, if larger), then the lists'
+size_t router_part_bytes(int T, int H, int E) {
+  moe::DeviceInfo dev;
+  if (T < 1 || H < 8 || E < 1 || moe::current_device(&dev) != MOE_OK) return 0;
+  const size_t a = moe_router_logits_workspace(T, H, E), b = moe::router_partials_bytes(T, H, E, dev.sm_count);
+  const size_t n = a > b ? a : b;
+  return (n + 255) / 256 * 256;
+}
+}  // namespace
 
 extern "C" size_t moe_route_finalize_workspace(int T, int H, int E, int K) {
-  return moe_router_logits_workspace(T, H, E) + moe_build_routing_lists_workspace(T, K, E);
+  return router_part_bytes(T, H, E) + moe_build_routing_lists_workspace(T, K, E);
 }
 
 extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const float* bias, const uint16_t* latent,
@@ -18,17 +29,30 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
                                   float scale, float* logits, int32_t* ids, float* weights, uint16_t* weights_bf16,
                                   int32_t* offsets, int32_t* pairs, uint8_t* q, uint8_t* scales, uint16_t* out,
                                   void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  using namespace moe;
   if (T < 1 || K < 1 || !weights_bf16) return MOE_ERR_INVALID_ARGUMENT;
-  const size_t rws = moe_router_logits_workspace(T, H, E);
+  if (E < 1 || H < 8 || H % 8 != 0 || (long long)T * E > (1LL << 40)) return MOE_ERR_INVALID_ARGUMENT;
+  if (!x || !w || !logits) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(logits, 4)) return MOE_ERR_ALIGNMENT;
+  const size_t rws = router_part_bytes(T, H, E);
   const size_t lws = moe_build_routing_lists_workspace(T, K, E);
   if (workspace_bytes < rws + lws || (rws + lws > 0 && !workspace)) return MOE_ERR_WORKSPACE;
+  if (rws > 0 && !aligned(workspace, 16)) return MOE_ERR_WORKSPACE;
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != MOE_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int st = moe_router_logits(x, w, logits, T, H, E, ws, rws, stream);
+  // The router stores its split-K partials and the top-K launch sums them (in split
+  // order, as the router's own reduction would: the same logits, bit for bit), so the
+  // router skips its on-chip exchange; with one split it writes the logits itself.
+  int S = 1;
+  float* part = reinterpret_cast<float*>(ws);
+  st = launch_router_partials(x, w, logits, T, H, E, dev.sm_count, part, dev.error_word, as_cuda(stream), &S);
   if (st != MOE_OK) return st;
   // the latent is an input of the step, complete before the router started: the
   // quantisation CTAs run beside the router instead of after it
-  st = moe::route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q,
-                           scales, true, moe::as_cuda(stream));
+  st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
+                      true, as_cuda(stream), S > 1 ? part : nullptr, S);
   if (st != MOE_OK) return st;
   st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws : nullptr, lws, stream);
   if (st != MOE_OK) return st;

@@ -29,10 +29,13 @@ int prefer_max_shared(const void* func);
 // Sigmoid top-K and MXFP8 of the latent in one launch (moe_topk_route_quantize). With
 // latent_ready the quantisation CTAs do not wait for the preceding kernel: only for a
 // latent complete before that kernel started, and a preceding kernel that signals its
-// dependents after its own wait (the router kernels do).
+// dependents after its own wait (the router kernels do). With part != nullptr the
+// logits are not read but made: the sum in split order of the router's S partials
+// part [S][T][E], written to `logits` (which is then an output).
 int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
-                   uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s);
+                   uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part = nullptr,
+                   int S = 0);
 
 // Finalize (moe_finalize). With inputs_ready the kernel does not wait for the preceding
 // kernel: only when rows, weights and indices were complete before that kernel was

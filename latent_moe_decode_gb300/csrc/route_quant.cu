@@ -22,7 +22,7 @@ namespace {
 using namespace topk_impl;
 constexpr int kQuantUnroll = 8;  // 128 threads x 8 chunks = 16 KB per quantisation CTA
 
-template <int NJ>
+template <int NJ, bool PART>
 __global__ void __launch_bounds__(kThreads) route_quant_kernel(const TopkArgs a, const uint16_t* __restrict__ x,
                                                                long long nchunks, uint8_t* __restrict__ q,
                                                                uint8_t* __restrict__ scales, uint32_t* err, int qblocks,
@@ -32,11 +32,11 @@ __global__ void __launch_bounds__(kThreads) route_quant_kernel(const TopkArgs a,
   // otherwise the routing CTAs (the longer ones) come first.
   const int b = (int)blockIdx.x;
   if (quant_wait) {
-    if (b < a.T) topk_token<NJ>(a, b);
+    if (b < a.T) topk_token<NJ, PART>(a, b);
     else mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)(b - a.T), true);
   } else {
     if (b < qblocks) mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)b, false);
-    else topk_token<NJ>(a, b - qblocks);
+    else topk_token<NJ, PART>(a, b - qblocks);
   }
 }
 
@@ -47,7 +47,7 @@ namespace moe {
 
 int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
-                   uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s) {
+                   uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part, int S) {
   using namespace moe::topk_impl;
   if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARGUMENT;
   if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK) return MOE_ERR_CAPACITY;
@@ -65,12 +65,22 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
+  if (part) {
+    if (S < 1 || !aligned(part, 4)) return MOE_ERR_INVALID_ARGUMENT;
+    a.part = part;
+    a.S = S;
+    a.logits_out = const_cast<float*>(logits);
+    a.discard = (E % 32 == 0 && aligned(part, 128)) ? 1 : 0;
+  }
   const dim3 grid((unsigned)(T + qblocks)), block(kThreads);
   const int qb = (int)qblocks, qw = latent_ready ? 0 : 1;
   switch ((E + 127) / 128) {
-#define MOE_RQ_CASE(N) \
-  case N:              \
-    return launch_pdl(route_quant_kernel<N>, grid, block, 0, s, a, latent, nchunks, q, scales, dev.error_word, qb, qw);
+#define MOE_RQ_CASE(N)                                                                                     \
+  case N:                                                                                                   \
+    return part ? launch_pdl(route_quant_kernel<N, true>, grid, block, 0, s, a, latent, nchunks, q, scales,     \
+                             dev.error_word, qb, qw)                                                         \
+                : launch_pdl(route_quant_kernel<N, false>, grid, block, 0, s, a, latent, nchunks, q, scales,    \
+                             dev.error_word, qb, qw);
     MOE_RQ_CASE(1)
     MOE_RQ_CASE(2)
     MOE_RQ_CASE(3)

@@ -41,6 +41,12 @@ size_t front_workspace(const TcPlan& p, int T, int E, int L);
 int launch_front_tc(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* logits, uint16_t* latent, int T,
                     int H, int E, int L, const TcPlan& p, float* part, uint32_t* err, cudaStream_t stream);
 
+// The tensor-core router's split-K partials [S][T][E] without their reduction (the
+// consumer sums them in split order; S == 1: logits written directly). *S_out = S.
+int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int sm_count,
+                           float* part, uint32_t* err, cudaStream_t stream, int* S_out);
+size_t router_partials_bytes(int T, int H, int E, int sm_count);
+
 // logits = sum over s of part[s] (split order), part [S][T][E].
 int launch_router_reduce(const float* part, int S, int T, int E, float* logits, cudaStream_t stream);
 

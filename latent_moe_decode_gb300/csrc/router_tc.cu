@@ -487,7 +487,7 @@ int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* d
   // kernels after the router still launch early: it signals them.)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 * p.S : (CLUSTER ? p.S : 1);
+  attr[0].val.clusterDim.x = PAIR ? (CLUSTER ? 2 * p.S : 2) : (CLUSTER ? p.S : 1);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -699,6 +699,49 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
 // The front launch runs CTA pairs over pairs of 128-row tiles (both weights' tiles in
 // one sequence: a pair may hold the last router tile and the first latent tile). Its
 // splits are reduced only on chip: a cluster of S pairs, or no split.
+// The router's split-K partials without their reduction: the plan of tc_plan with the
+// splits not reduced on chip; each split CTA stores its FP32 partial to part [S][T][E]
+// and the consumer sums them in split order (moe_route_finalize: the top-K launch), which
+// gives the same sums as the cluster reduction, bit for bit. Only for wide token tiles,
+// whose on-chip exchange is the expensive one (5-6 us at T = 1020); narrow tiles (64
+// columns or fewer, up to 16 splits) keep their one-round-trip column reduction, which
+// costs less than 16 partials read by the consumer. Then, as with one split, the logits
+// are written to `logits` directly and *S_out = 1; otherwise *S_out = S.
+int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int sm_count,
+                           float* part, uint32_t* err, cudaStream_t stream, int* S_out) {
+  TcPlan p = tc_plan(T, H, E, sm_count);
+  if (p.S == 1 || p.bn <= 64) {
+    *S_out = 1;
+    return launch_router_tc(x, w, logits, T, H, E, p, part, err, stream);
+  }
+  *S_out = p.S;
+  float* dst = p.S > 1 ? part : logits;
+  p.cluster = false;
+  int st = MOE_ERR_INVALID_ARGUMENT;
+#define MOE_TC_PART_CASE(B)                                                                                     \
+  case B:                                                                                                        \
+    st = p.pair ? launch_bn<B, false, false, true>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream) \
+                : launch_bn<B, false, false, false>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream); \
+    break;
+  switch (p.bn) {
+    case 16:
+      st = launch_bn<16, false, false, false>(x, w, nullptr, dst, nullptr, part, T, H, E, 0, p, err, stream);
+      break;
+    MOE_TC_PART_CASE(32)
+    MOE_TC_PART_CASE(64)
+    MOE_TC_PART_CASE(128)
+    MOE_TC_PART_CASE(256)
+    default: break;
+  }
+#undef MOE_TC_PART_CASE
+  return st;
+}
+
+size_t router_partials_bytes(int T, int H, int E, int sm_count) {
+  const TcPlan p = tc_plan(T, H, E, sm_count);
+  return (p.S > 1 && p.bn > 64) ? (size_t)p.S * T * E * sizeof(float) : 0;
+}
+
 TcPlan front_plan(int T, int H, int E, int L, int sm_count) {
   return pair_plan(T, H, (E + kBM - 1) / kBM + (L + kBM - 1) / kBM, sm_count);
 }

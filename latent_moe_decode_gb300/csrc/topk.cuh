@@ -92,13 +92,22 @@ struct TopkArgs {
   int32_t* ids;
   float* weights;
   uint16_t* weights_bf16;
+  // Optional: the router's split-K partials [S][T][E] instead of logits. Each token's
+  // logits are then their sum in split order (as the router's own reduction), written
+  // to logits_out; the partial lines read are invalidated in L2 when discard is set.
+  const float* part = nullptr;
+  int S = 0;
+  float* logits_out = nullptr;
+  int discard = 0;
 };
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 
-// One token's selection, run by a CTA of kThreads threads.
-template <int NJ>
+// One token's selection, run by a CTA of kThreads threads. PART: the logits are summed
+// from the router's split-K partials (a.part) and written (a.logits_out); a separate
+// instantiation, so the plain selection keeps its register count (and occupancy).
+template <int NJ, bool PART = false>
 __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
   __shared__ uint32_t s_top[kWarps][32];
   __shared__ int s_cnt[kWarps];
@@ -119,10 +128,48 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
   // 1) approximate keys of this thread's experts tid + 128 j
   uint32_t key[NJ];
   float x[NJ], b[NJ];
+  if constexpr (PART) {
+    // the logits: the S partials summed in split order, 4 splits' loads in flight at once
+    constexpr int kSG = 4;
+    for (int s0 = 0; s0 < a.S; s0 += kSG) {
+      float p[kSG][NJ];
+#pragma unroll
+      for (int i = 0; i < kSG; ++i)
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int e = tid + 128 * j;
+          p[i][j] = (s0 + i < a.S && e < E) ? __ldcg(a.part + ((size_t)(s0 + i) * a.T + t) * E + e) : 0.f;
+        }
+#pragma unroll
+      for (int i = 0; i < kSG; ++i)
+        if (s0 + i < a.S)
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) x[j] = s0 + i == 0 ? p[i][j] : __fadd_rn(x[j], p[i][j]);
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = tid + 128 * j;
+      if (e < E) a.logits_out[(size_t)t * E + e] = x[j];
+    }
+    __syncwarp();  // every lane's loads are consumed before their lines are invalidated
+    if (a.discard) {  // whole 128-byte lines of this warp's experts (E % 32 == 0, aligned)
+      for (int l = lane; l < a.S * NJ; l += 32) {
+        const int s = l / NJ, j = l - s * NJ;
+        const int e0 = 32 * warp + 128 * j;
+        if (e0 < E)
+          asm volatile("discard.global.L2 [%0], 128;" ::"l"(a.part + ((size_t)s * a.T + t) * E + e0) : "memory");
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = tid + 128 * j;
+      x[j] = e < E ? __ldg(lg + e) : 0.f;
+    }
+  }
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int e = tid + 128 * j;
-    x[j] = e < E ? __ldg(lg + e) : 0.f;
     b[j] = (a.bias && e < E) ? __ldg(a.bias + e) : 0.f;
   }
   uint32_t tmax = 0;

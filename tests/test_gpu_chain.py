@@ -80,9 +80,12 @@ def test_wide_in_cuda_graph(moe, orc):
     _check_chain(moe, orc, 1020, samples=2000, graph=True)
 
 
-@pytest.mark.parametrize("T", [8, 1020])
+@pytest.mark.parametrize("T", [1, 8, 64, 100, 256, 1020, 2048, 4096])
 def test_one_call_equals_four_calls(moe, T):
-    """moe_route_finalize == the four calls it stands for, every output bit for bit."""
+    """moe_route_finalize == the four calls it stands for, every output bit for bit --
+    including the logits, which the one call's top-K launch sums from the router's
+    split-K partials (every router plan: 16 splits of narrow tiles, 64- and 128-column
+    tiles, 5-CTA clusters, CTA pairs with and without splits)."""
     d = synth.chain_inputs(T, seed=3)
     x, w, bias, latent, rows = bf16_dev(d["x"]), bf16_dev(d["w"]), dev(d["bias"]), bf16_dev(d["latent"]), bf16_dev(d["rows"])
     one = moe.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K)
