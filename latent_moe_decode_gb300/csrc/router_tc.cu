@@ -358,60 +358,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t < T) store_out<FRONT>(out, out2, t, mt, mt1, r, E, L, acc);
         }
       }
-    } else {
-    if (done && live) {
+    } else {  // wide tiles: owners of units
+      if (done && live) {
 #pragma unroll 1
-      for (int ch = wg; ch < nch; ch += kGroups) {
-        if (mine(ch)) continue;
-        uint32_t v[16];
-        tmem_ld16(tl + (uint32_t)(16 * ch), v);
-        tmem_wait_ld();
+        for (int ch = wg; ch < nch; ch += kGroups) {
+          if (mine(ch)) continue;
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)(16 * ch), v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) __stcg(slot + (size_t)(16 * ch + j) * kBM + row, __uint_as_float(v[j]));
-      }
-    }
-    cluster_sync();  // every split's partial chunks are written and visible to the cluster
-    if (done && live) {
-#pragma unroll 1
-      for (int ch = my0 / 4 + wg; ch < (my1 + 3) / 4; ch += kGroups) {
-        if (!mine(ch)) continue;  // (warp-uniform)
-        uint32_t v[16];
-        tmem_ld16(tl + (uint32_t)(16 * ch), v);
-        tmem_wait_ld();
-        float acc[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {  // split order (S <= 8 here); a split's 16 columns loaded at once
-          if (q >= S) break;
-          float p[16];
-          if (q == s) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) p[j] = __uint_as_float(v[j]);
-          } else {
-            const float* src = part + ((tile * S + q) * (size_t)BN + 16 * ch) * kBM + row;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) p[j] = __ldcg(src + (size_t)j * kBM);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = q == 0 ? p[j] : __fadd_rn(acc[j], p[j]);
-        }
-        __syncwarp();  // every lane's loads are consumed before their lines are invalidated
-        if (discard && lane < 16) {  // (a workspace aligned to 128 bytes: whole lines)
-          for (int q = 0; q < S; ++q) {
-            if (q == s) continue;
-            const float* line = part + ((tile * S + q) * (size_t)BN + 16 * ch + lane) * kBM + (warp & 3) * 32;
-            asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = nt * BN + 16 * ch + j;
-          if (t < T) store_out<FRONT>(out, out2, t, mt, mt1, row, E, L, acc[j]);
+          for (int j = 0; j < 16; ++j) __stcg(slot + (size_t)(16 * ch + j) * kBM + row, __uint_as_float(v[j]));
         }
       }
+      cluster_sync();  // every split's partial chunks are written and visible to the cluster
+      if (done && live) {
+#pragma unroll 1
+        for (int ch = my0 / 4 + wg; ch < (my1 + 3) / 4; ch += kGroups) {
+          if (!mine(ch)) continue;  // (warp-uniform)
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)(16 * ch), v);
+          tmem_wait_ld();
+          float acc[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {  // split order (S <= 8 here); a split's 16 columns loaded at once
+            if (q >= S) break;
+            float p[16];
+            if (q == s) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) p[j] = __uint_as_float(v[j]);
+            } else {
+              const float* src = part + ((tile * S + q) * (size_t)BN + 16 * ch) * kBM + row;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) p[j] = __ldcg(src + (size_t)j * kBM);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = q == 0 ? p[j] : __fadd_rn(acc[j], p[j]);
+          }
+          __syncwarp();  // every lane's loads are consumed before their lines are invalidated
+          if (discard && lane < 16) {  // (a workspace aligned to 128 bytes: whole lines)
+            for (int q = 0; q < S; ++q) {
+              if (q == s) continue;
+              const float* line = part + ((tile * S + q) * (size_t)BN + 16 * ch + lane) * kBM + (warp & 3) * 32;
+              asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = nt * BN + 16 * ch + j;
+            if (t < T) store_out<FRONT>(out, out2, t, mt, mt1, row, E, L, acc[j]);
+          }
+        }
+      }
     }
-    }  // BN > 64
   } else if (done) {
-    float* dst = out + (size_t)s * T * E;  // (FRONT plans have S == 1)
+    // the logits (S == 1), or split s's partial of part [S][T][E] for a consumer that sums
+    // them (the routing step's top-K launch; FRONT plans have S == 1)
+    float* dst = out + (size_t)s * T * E;
 #pragma unroll 1
     for (int c0 = 16 * wg; c0 < BN; c0 += 16 * kGroups) {
       uint32_t v[16];
