@@ -360,9 +360,12 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  *   moe_build_routing_lists(ids, T, K, E, offsets, pairs)
  *   moe_finalize(rows, T*K, NULL, weights_bf16, MOE_DTYPE_BF16, NULL, 1, T, K, L, out)
  * i.e. Finalize combines the expanded expert rows (row t*K + k = token t's k-th
- * expert) with the BF16 routing weights, as the wide page's Finalize does. Arguments,
- * layouts and requirements are those of the four calls (weights may be NULL;
- * weights_bf16 may not). `workspace` holds moe_route_finalize_workspace(T, H, E, K)
+ * expert) with the BF16 routing weights, as the wide page's Finalize does. Every
+ * output equals the four calls' bit for bit. (For token tiles wider than 64 the router
+ * stores its split-K partials in the workspace instead of reducing them, and the top-K
+ * launch sums each token's partials in the same split order before selecting: the
+ * same logits, one on-chip exchange fewer.) Arguments, layouts and requirements are
+ * those of the four calls (weights may be NULL; weights_bf16 may not). `workspace` holds moe_route_finalize_workspace(T, H, E, K)
  * bytes (NULL when that is 0); it is clobbered. Returns the first non-OK status of the
  * four calls (the later ones are then not launched). Allocates nothing, so the call
  * can be captured in a CUDA graph.
