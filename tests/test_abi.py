@@ -86,6 +86,9 @@ def test_validation_before_any_cuda_call(lib):
     assert chain(0, 16, A16) == 1
     assert chain(8, 0, A16) == 1
     assert chain(8, 16, None) == 1
+    bad_x = lambda: lib.moe_route_finalize(P(264), A16, None, A16, A16, 8, 7168, 3584, 896, 16, 1, 1.0, A16, A16,
+                                           None, A16, A16, A16, A16, A16, A16, None, 0, None)
+    assert bad_x() == 2  # the step checks x itself (its router is launched directly)
     assert lib.moe_router_logits_ex(P(264), A16, A16, 8, 7168, 896, None, 0, 0, None) == 2
     assert lib.moe_build_unit_windows(A16, 0, 8, A16, A16, A16, A16, 4, None) == 1
     assert lib.moe_build_unit_windows(A16, 896, 0, A16, A16, A16, A16, 4, None) == 1
