@@ -744,27 +744,43 @@ size_t router_partials_bytes(int T, int H, int E, int sm_count) {
   return (p.S > 1 && p.bn > 64) ? (size_t)p.S * T * E * sizeof(float) : 0;
 }
 
+// Both weights' 128-row tiles in one sequence, on CTA pairs or single CTAs, whichever
+// keeps more SMs busy (at small T pairs need 8-CTA clusters of which too few fit at
+// once; single CTAs split K over up to 16). Splits are reduced only on chip.
 TcPlan front_plan(int T, int H, int E, int L, int sm_count) {
-  return pair_plan(T, H, (E + kBM - 1) / kBM + (L + kBM - 1) / kBM, sm_count);
+  const int m_tiles = (E + kBM - 1) / kBM + (L + kBM - 1) / kBM;
+  const TcPlan pair = pair_plan(T, H, m_tiles, sm_count);
+  TcPlan single = tc_plan_single(T, H, m_tiles * kBM, sm_count);
+  if (single.S > 1 && !single.cluster) single.S = 1;
+  return plan_ctas(pair, T, m_tiles) >= plan_ctas(single, T, m_tiles) ? pair : single;
 }
 
 size_t front_workspace(const TcPlan& p, int T, int E, int L) {
-  const int pairs = ((E + kBM - 1) / kBM + (L + kBM - 1) / kBM + 1) / 2;
-  return tc_workspace(p, T, 2 * pairs * kBM);
+  return tc_workspace(p, T, ((E + kBM - 1) / kBM + (L + kBM - 1) / kBM) * kBM);  // (pairs: rounded to even)
 }
 
 int launch_front_tc(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* logits, uint16_t* latent, int T,
                     int H, int E, int L, const TcPlan& p, float* part, uint32_t* err, cudaStream_t stream) {
-  if ((p.S > 1 && !p.cluster) || !p.pair) return MOE_ERR_INVALID_ARGUMENT;
-#define MOE_TC_CASE(B)                                                                                         \
+  if (p.S > 1 && !p.cluster) return MOE_ERR_INVALID_ARGUMENT;
+#define MOE_TC_CASE(B, PR)                                                                                     \
   case B:                                                                                                       \
-    return p.cluster ? launch_bn<B, true, true, true>(x, w, w2, logits, latent, part, T, H, E, L, p, err, stream) \
-                     : launch_bn<B, false, true, true>(x, w, w2, logits, latent, part, T, H, E, L, p, err, stream);
+    return p.cluster ? launch_bn<B, true, true, PR>(x, w, w2, logits, latent, part, T, H, E, L, p, err, stream) \
+                     : launch_bn<B, false, true, PR>(x, w, w2, logits, latent, part, T, H, E, L, p, err, stream);
+  if (p.pair) {
+    switch (p.bn) {
+      MOE_TC_CASE(32, true)
+      MOE_TC_CASE(64, true)
+      MOE_TC_CASE(128, true)
+      MOE_TC_CASE(256, true)
+      default: return MOE_ERR_INVALID_ARGUMENT;
+    }
+  }
   switch (p.bn) {
-    MOE_TC_CASE(32)
-    MOE_TC_CASE(64)
-    MOE_TC_CASE(128)
-    MOE_TC_CASE(256)
+    MOE_TC_CASE(16, false)
+    MOE_TC_CASE(32, false)
+    MOE_TC_CASE(64, false)
+    MOE_TC_CASE(128, false)
+    MOE_TC_CASE(256, false)
     default: return MOE_ERR_INVALID_ARGUMENT;
   }
 #undef MOE_TC_CASE
