@@ -2,13 +2,13 @@
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.layer,
 // EpMoeLayer (the FP32-output split-K router projection of the [896, 7168] BF16 gate,
-// "split-K reduces in FP32") and front_tactic (64-row weight tiles, a token tile of the
+// its split-K partials reduced in FP32) and front_tactic (64-row weight tiles, a token tile of the
 // next size in {8, 16, 32, 64, 128} at or above the batch, the deepest pipeline that
 // fits in about 200 KiB of shared memory, 256-byte K steps).
 //
 // GB300 design: logits^T = W x^T, i.e. the MMA's M dimension runs over experts and its
 // N dimension over tokens, so a decode batch of 8..256 tokens is one N tile and the
-// gate is the streamed operand. One CTA (4 warps) computes a 128-expert x BN-token
+// gate is the streamed operand. One CTA (16 warps) computes a 128-expert x BN-token
 // tile over a range of 64-wide K blocks:
 //   - warp 0, one lane: TMA producer. Each stage is a 128x64 BF16 gate tile and a
 //     BNx64 BF16 token tile, both 128-byte swizzled (K-major), landed on a full
@@ -33,6 +33,12 @@
 // store), and the workspace lines read are invalidated in L2 (discard.global.L2), so
 // the scratch never costs an HBM write-back. Otherwise the partials [S][T][E] go to
 // the workspace and a second kernel sums them in split order.
+// Variants of the same kernel: PAIR, two CTAs on two SMs running one M = 256 MMA
+// (cta_group::2) over their 128-row tiles, each staging half the token rows (for wide
+// batches: a third fewer bytes per SM for the same MMA work); FRONT, a second weight
+// (the latent down projection) whose tiles follow the router's and store BF16 rows (the
+// front projection); and the step's partials mode (no cluster, S > 1: the partials
+// [S][T][E] are summed by the top-K launch of the one-call step).
 // Every mbarrier wait is bounded by the global timer; on expiry the kernel sets
 // MOE_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies in flight,
 // frees its TMEM and exits.
