@@ -81,8 +81,8 @@ int moe_device_error(uint32_t* bits, int clear);
  * Router logits.
  *   logits[t, e] = sum_j x[t, j] * w[e, j]      (FP32 accumulate and output, no bias)
  * Source: [ep] EpMoeLayer.stock_order (mm(x, gate^T) with an FP32 output) and
- * EpMoeLayer.__init__ (the FP32-output split-K router projection, "split-K reduces in
- * FP32", module docstring); [wide] module docstring ("FP32 router logits").
+ * EpMoeLayer.__init__ (the FP32-output split-K router projection, its partials reduced
+ * in FP32, module docstring); [wide] module docstring (the router logits are FP32).
  *
  *   x         device, BF16 [T, H]        hidden rows
  *   w         device, BF16 [E, H]        router weight (gate), expert rows
@@ -167,8 +167,8 @@ int moe_front_projection(const uint16_t* x, const uint16_t* w_router, const uint
 /* -------------------------------------------------------------------------------
  * Sigmoid + e_score_correction_bias top-K with renormalised weights.
  * Source: [ep] EpMoeLayer.topk (one group, sigmoid scoring, correction bias,
- * renormalize, routed scaling); [wide] WideRoute docstring ("exact top16 and
- * renormalized weights"); [wide] WideMoE.__init__ (bias, renorm, scale taken from the
+ * renormalize, routed scaling); [wide] WideRoute docstring (an exact top-16 with
+ * renormalised weights); [wide] WideMoE.__init__ (bias, renorm, scale taken from the
  * module); [wide] WideScratch (ids int32 [cap, 16], weights BF16 [cap, 16]).
  *
  * Per token t:
@@ -263,7 +263,7 @@ int moe_build_unit_windows(const int32_t* offsets, int E, int window, int32_t* u
 
 /* -------------------------------------------------------------------------------
  * MXFP8 (OCP Microscaling) quantisation of BF16 rows.
- * Source: [wide] module docstring ("MXFP8 activations") and WideRoute (the token's
+ * Source: [wide] module docstring (the activations are MXFP8) and WideRoute (the token's
  * MXFP8 plan row written from its BF16 latent); [ep] module docstring ("the MXFP8
  * latent"). Read as OCP MX v1.0: per block of 32 consecutive elements of a row,
  *   se = clamp(floor(log2(max |v|)) - 8, -127, 127),   scale byte = se + 127 (E8M0),

@@ -1,8 +1,8 @@
 // MXFP8 (OCP Microscaling) quantisation of BF16 rows.
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide (module
-// docstring: "MXFP8 activations"; WideRoute: a token's MXFP8 plan row is written from
-// its BF16 latent) and ...moe.ep.layer (module docstring: "the MXFP8 latent"). The
+// docstring: MXFP8 activations; WideRoute: a token's MXFP8 plan row is written from
+// its BF16 latent) and ...moe.ep.layer (module docstring: the latent in MXFP8). The
 // pages fix no more than "MXFP8"; the OCP MX v1.0 reading is: per block of 32
 // consecutive elements, scale exponent se = floor(log2 amax) - 8 (8 = emax of E4M3)
 // clamped to [-127, 127] and stored as the E8M0 byte se + 127; elements E4M3(v / 2^se),

@@ -2,7 +2,7 @@
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.layer,
 // EpMoeLayer (the FP32-output split-K router projection of the [896, 7168] BF16 gate:
-// split 4 for up to 32 tokens, 64-row weight tiles, "split-K reduces in FP32") and
+// split 4 for up to 32 tokens, 64-row weight tiles, split-K partials reduced in FP32) and
 // EpMoeLayer.stock_order (mm(x, gate^T) with an FP32 output).
 //
 // GB300 design: at a handful of tokens the router is one pass over the 12.8 MB weight,

@@ -3,7 +3,7 @@
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.layer,
 // EpMoeLayer.topk (one group, sigmoid scoring, correction bias, renormalize, scale);
 // vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideRoute docstring
-// ("exact top16 and renormalized weights") and WideScratch (ids int32, weights BF16).
+// (an exact top-16 with renormalised weights) and WideScratch (ids int32, weights BF16).
 //
 // Selection key c_e = sigmoid(logit_e) + bias_e; order (c descending, expert index
 // ascending); weights are the unbiased scores over their slot-order FP32 sum.

@@ -61,8 +61,8 @@ static float f32_from_bits(uint32_t u) {
 /* ------------------------------------------------------------------------- */
 /* Router logits.
  * [ep] EpMoeLayer.stock_order: logits = mm(x, gate^T) with out_dtype float32; the
- * [ep] module docstring: "FP32 router logits", "split-K reduces in FP32";
- * [wide] module docstring: "FP32 router logits".
+ * [ep] module docstring: the router logits are FP32 and the split-K partials are reduced in FP32;
+ * [wide] module docstring: FP32 router logits.
  * The oracle is the tolerance reference: the exact products of BF16 values summed
  * in FP64, plus sum_j |x*w| as the forward-error denominator. */
 void oracle_router_logits(const uint16_t* x, const uint16_t* w, int T, int H, int E,
@@ -203,7 +203,7 @@ void oracle_sigmoid_array(const float* x, float* out, long n) {
 /* Sigmoid + e_score_correction_bias top-k with renormalised weights.
  * [ep] EpMoeLayer.topk: fused_grouped_topk(x, logits, 16, renormalize, bias, 1, 1,
  *      "sigmoid", scale) -- one group, sigmoid scores, bias-corrected selection.
- * [wide] WideRoute docstring: "exact top16 and renormalized weights".
+ * [wide] WideRoute docstring: an exact top-16 with renormalised weights.
  * [wide] WideMoE.__init__: bias = gate.e_score_correction_bias, scale =
  *      routed_scaling_factor, renorm = moe_renormalize.
  * Readings where the pages are silent: selection key c_e = s_e + bias_e (FP32 add);
@@ -331,8 +331,8 @@ int oracle_unit_windows(const int32_t* offsets, int E, int window, int32_t* unit
 
 /* ------------------------------------------------------------------------- */
 /* MXFP8 quantisation of BF16 rows.
- * [wide] module docstring: "MXFP8 activations"; [ep] module docstring: "the MXFP8
- * latent (bit-identical to mxfp8_quantize)"; [wide] WideRoute: the plan row of a
+ * [wide] module docstring: MXFP8 activations; [ep] module docstring: the latent in MXFP8,
+ * bit-identical to the stock mxfp8_quantize; [wide] WideRoute: the plan row of a
  * token is written from its BF16 latent. The pages define no further detail, so the
  * OCP Microscaling (MX) v1.0 reading is taken: blocks of 32 consecutive elements,
  * one E8M0 scale X = 2^se with se = floor(log2(amax)) - emax(E4M3) = floor(log2 amax) - 8,

@@ -1,5 +1,5 @@
 """MXFP8 quantisation on the GPU against the oracle, bit for bit (OCP MX reading of
-the pages' "MXFP8 activations")."""
+the pages' MXFP8 activations)."""
 import numpy as np
 import pytest
 import torch

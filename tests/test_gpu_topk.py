@@ -1,6 +1,6 @@
 """Sigmoid + bias top-K on the GPU against the oracle (which consumes the same
 logits): ids, FP32 and BF16 weights bit for bit (DEP page, EpMoeLayer.topk; wide
-page, WideRoute "exact top16 and renormalized weights")."""
+page, WideRoute an exact top-16 with renormalised weights)."""
 import os
 from concurrent.futures import ThreadPoolExecutor
 

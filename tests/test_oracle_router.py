@@ -1,4 +1,4 @@
-"""Pins of the oracle's FP64 router logits ("FP32 router logits" of the wide and DEP
+"""Pins of the oracle's FP64 router logits (FP32 router logits of the wide and DEP
 pages: logits = x @ gate^T) against exact integer arithmetic and an independent
 FP64 matmul."""
 import numpy as np

@@ -1,6 +1,6 @@
 """Pins of the oracle's sigmoid+bias top-k ("EpMoeLayer.topk" of the DEP page: one
-group, sigmoid scoring, correction bias, renormalize, scale; "exact top16 and
-renormalized weights" of the wide page's WideRoute) against closed forms and a
+group, sigmoid scoring, correction bias, renormalize, scale; the wide page's WideRoute: an
+exact top-16 with renormalised weights) against closed forms and a
 brute-force sort."""
 import numpy as np
 import pytest
