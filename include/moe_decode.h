@@ -121,8 +121,13 @@ int moe_router_logits_ex(const uint16_t* x, const uint16_t* w, float* logits, in
  *   - The first call on a device looks up the array's device address with that device
  *     current (cudaGetSymbolAddress) and caches it; make that first call before any
  *     stream capture.
- *   - Sizes whose partials would not fit (moe_router_logits_workspace(T, H, E) above
- *     the limit) return MOE_ERR_CAPACITY and launch nothing. With E = 896 every T fits.
+ *   - Sizes whose tensor-core split-K partials would not fit in the array, and
+ *     T * E > 2^40 as for moe_router_logits, return MOE_ERR_CAPACITY and launch
+ *     nothing. The tensor-core plan keeps (splits x token tiles x 128-expert tiles) at
+ *     or below the SM count and a tile's partial at or below 256 x 128 FP32, so its
+ *     partials never exceed SM count x 128 KiB: 19 MiB on a 152-SM GB300, inside the
+ *     20 MiB array for every T and E. (moe_router_logits_workspace may report more: it
+ *     also covers the CUDA-core family, which this call never runs.)
  *   - Every call on a device shares the array and leaves its contents behind; nothing
  *     in it needs to start at zero. Calls whose kernels overlap on the GPU (other
  *     streams, other threads) race on it: order them on one stream.
@@ -198,9 +203,9 @@ int moe_topk_route(const float* logits, const float* bias, int T, int E, int K, 
                    moe_stream_t stream);
 
 /* moe_topk_route and mxfp8_quantize_rows(latent, rows, cols, q, scales) in ONE launch
- * ([wide] WideRoute: one launch of 2b CTAs, CTA t routes token t, CTA b + t writes the
- * MXFP8 plan row of token t): the quantisation CTAs stream the latent on the SMs the
- * selection leaves free. Results are identical to the two separate calls; arguments
+ * ([wide] WideRoute: the top-K CTAs and the latent-quantisation CTAs of a batch share
+ * one grid): the quantisation CTAs stream the latent on the SMs the selection leaves
+ * free. Results are identical to the two separate calls; arguments
  * and requirements are theirs (T >= 1; rows may be 0). */
 int moe_topk_route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize,
                             float scale, int32_t* ids, float* weights, uint16_t* weights_bf16,

@@ -1,9 +1,11 @@
 // The routing-and-combine step as one call: the four launches of the chain, in order,
 // on the caller's stream. The router is launched the ordinary way (it starts once its
 // predecessor has completed) and signals its dependents after that; the later kernels
-// use programmatic dependent launch and wait for their predecessor only before reading
-// what the chain wrote -- the MXFP8 CTAs (a step input) not at all, Finalize only at
-// its end, so it streams its rows while the lists kernel runs.
+// use programmatic dependent launch and execute griddepcontrol.wait before they read
+// anything an earlier kernel of the step wrote. Reads of the step's own inputs may come
+// first: the MXFP8 CTAs quantise the latent without waiting, and Finalize issues its
+// first row copies before its wait (and reads top-K's weights only after it), so the
+// rows stream in while the lists kernel runs.
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideMoE.run
 // (router -> route -> Finalize on one stream) and ...moe.ep.layer, EpMoeLayer.__call__.
@@ -56,9 +58,8 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   if (st != MOE_OK) return st;
   st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws : nullptr, lws, stream);
   if (st != MOE_OK) return st;
-  // Finalize reads only the step's rows and top-K's weights, both complete once the lists
-  // kernel has passed its own wait (it signals its dependents only then): Finalize runs
-  // beside the lists instead of after them.
+  // Finalize starts its row copies (a step input) before its wait, and reads top-K's
+  // weights after it, once the lists kernel (which itself waited for top-K) is complete.
   return moe::finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out, true,
                        moe::as_cuda(stream));
 }

@@ -37,12 +37,13 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
                    uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part = nullptr,
                    int S = 0);
 
-// Finalize (moe_finalize). With inputs_ready the kernel does not wait for the preceding
-// kernel: only when rows, weights and indices were complete before that kernel was
-// launched (it runs beside it).
+// Finalize (moe_finalize). With rows_ready (no row_index) the first row copies are
+// issued before the kernel waits for its predecessor, and everything else (weights) is
+// read after the wait: only when the rows (and shared rows) were complete before the
+// preceding kernel started.
 int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, const void* weights, int weights_dtype,
              const uint16_t* shared, float routed_scaling_factor, int T, int K, int H, uint16_t* out,
-             bool inputs_ready, cudaStream_t s);
+             bool rows_ready, cudaStream_t s);
 
 inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 

@@ -13,16 +13,20 @@
 // fragment) so that a warp covers 512 contiguous bytes of each row. The grid is
 // persistent (as many CTAs as fit: three per SM at K = 16) and thread i of the grid
 // takes the fragments i, i + G, i + 2G, ... (G threads in the grid). Each thread runs
-// its own ring of kStages shared-memory stages: it issues the asynchronous 16-byte
-// copies (cp.async, bypassing L1, evict-first in L2) of all K row fragments of the
-// next fragment, and loads that fragment's K weights into registers, before it waits
-// for and sums the current one. HBM thus always has the next items in flight and the
+// its own ring of kStages shared-memory stages, each holding one item's K row
+// fragments, copied asynchronously (16-byte cp.async, bypassing L1, evict-first in
+// L2), and the item's K weights in registers. It waits for the oldest stage, sums it
+// (FP32 fma chain in k order, one 16-byte store) and refills that stage with the item
+// kStages ahead, so HBM always has kStages items of every thread in flight and the
 // stream does not drain between waves of CTAs; the weights, loaded one item ahead,
 // never add their latency to an item. Slots are private to their thread ([stage][k]
-// [thread]: conflict-free), so no CTA barrier is needed. Per fragment: wait for its
-// copy group, FP32 fma chain in k order, one 16-byte store. Two stages and three CTAs
-// per SM keep more bytes in flight than three stages and two CTAs (the shared memory
-// of an SM holds six items either way).
+// [thread]: conflict-free), so no CTA barrier is needed. Two stages and three CTAs per
+// SM keep more bytes in flight than three stages and two CTAs (the shared memory of
+// an SM holds six items either way).
+// When the rows are an input complete before the preceding kernel started (the
+// one-call step: the preceding kernels make only the weights), the first kStages
+// items' row copies are issued before griddepcontrol.wait and their weights are read
+// after it, so the first 30 MB of rows stream in while the preceding kernel finishes.
 #include "common.cuh"
 #include <type_traits>
 
@@ -41,7 +45,10 @@ struct FinArgs {
   int T, K, H;
   uint16_t* out;
   uint32_t* err;
-  int wait;  // wait for the preceding kernel before reading (0: the caller knows the inputs are ready)
+  // 1: wait for the preceding kernel before reading anything; 0: the rows (and the
+  // shared rows) were complete before the preceding kernel started, so the first row
+  // copies are issued before the wait, and the weights (and indices) after it
+  int wait_all;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
@@ -68,18 +75,17 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   const long long f0 = (long long)blockIdx.x * kThreads + threadIdx.x;
   const size_t H = (size_t)a.H;
   grid_launch_dependents();
-  if (a.wait) grid_wait();  // rows, weights and indices may come from the preceding kernel
+  // indices choose the rows to copy: with a gather, everything waits
+  const bool early = !a.wait_all && !GATHER;
+  if (!early) grid_wait();
   const uint64_t pol = policy_evict_first();
   const uint32_t base = smem_u32(slots) + threadIdx.x * 16u;
   const int SL = K + (SHARED ? 1 : 0);  // slots per stage: K rows, then the shared row
   const uint32_t stage_bytes = (uint32_t)SL * kThreads * 16u;
 
   // Copies of fragment fi's K row fragments (and its shared-row fragment) into stage
-  // st, as one commit group (empty past the end), and its K raw weights into wraw[st];
-  // returns the mask of rows not skipped.
-  using WRaw = typename std::conditional<BF16W, uint16_t, float>::type;
-  WRaw wraw[kStages][KM];
-  auto issue = [&](int st, long long fi) -> uint32_t {
+  // st, as one commit group (empty past the end); returns the mask of rows not skipped.
+  auto issue_rows = [&](int st, long long fi) -> uint32_t {
     uint32_t m = 0;
     if (fi < total) {
       const int t = (int)(fi / frags);
@@ -93,7 +99,6 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
             set_error(a.err, MOE_DEVERR_ROW_INDEX);
             r = -1;
           }
-          wraw[st][k] = __ldg(static_cast<const WRaw*>(a.weights) + ix);
           if (r != -1) {
             m |= 1u << k;
             cp_async16(base + (uint32_t)st * stage_bytes + (uint32_t)(k * kThreads * 16), a.rows + (size_t)r * H + col,
@@ -107,21 +112,35 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     cp_async_commit();
     return m;
   };
+  // fragment fi's K raw weights into wraw[st] (read one item ahead of their use)
+  using WRaw = typename std::conditional<BF16W, uint16_t, float>::type;
+  WRaw wraw[kStages][KM];
+  auto load_weights = [&](int st, long long fi) {
+    if (fi < total) {
+      const int t = (int)(fi / frags);
+#pragma unroll
+      for (int k = 0; k < KM; ++k)
+        if (KT || k < K) wraw[st][k] = __ldg(static_cast<const WRaw*>(a.weights) + (size_t)t * K + k);
+    }
+  };
 
+  // the first kStages items: rows first (before the wait when they are a step input),
+  // weights after the wait
   uint32_t mask[kStages];
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) mask[s] = issue(s, f0 + s * stride);
+  for (int s = 0; s < kStages; ++s) mask[s] = issue_rows(s, f0 + s * stride);
+  if (early) grid_wait();  // the weights may come from the preceding kernel
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) load_weights(s, f0 + s * stride);
+
   for (long long f = f0; f < total; f += kStages * stride) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       const long long fi = f + s * stride;
-      constexpr int kAhead = kStages - 1;
-      const int sn = (s + kAhead) % kStages;
-      mask[sn] = issue(sn, fi + kAhead * stride);
       if (fi >= total) break;
       const int t = (int)(fi / frags);
       const int col = (int)(fi - (long long)t * frags) * 8;
-      // the weights, loaded at issue, times routed_scaling_factor
+      // the weights, loaded one item ahead, times routed_scaling_factor
       float w[KM];
 #pragma unroll
       for (int k = 0; k < KM; ++k) {
@@ -132,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
         }
         w[k] = wk;
       }
-      cp_async_wait<kAhead>();
+      cp_async_wait<kStages - 1>();  // stage s has landed (the groups after it may not have)
       // FP32 fma over k in order
       float acc[8];
 #pragma unroll
@@ -158,6 +177,11 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
           acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(q4[q]));
         }
       }
+      // stage s is consumed (its values are in registers): refill it with the item
+      // kStages ahead, so kStages items stay in flight
+      const long long fn = fi + kStages * stride;
+      mask[s] = issue_rows(s, fn);
+      load_weights(s, fn);
       uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);
       o.y = pack_bf16x2(acc[2], acc[3]);
@@ -167,7 +191,6 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     }
   }
   cp_async_wait<0>();
-  if (!a.wait) grid_wait();  // not done before the preceding kernel: stream order holds for what follows
 }
 
 template <int KT, bool G, bool B, bool S>
@@ -207,7 +230,7 @@ namespace moe {
 
 int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, const void* weights, int weights_dtype,
              const uint16_t* shared, float routed_scaling_factor, int T, int K, int H, uint16_t* out,
-             bool inputs_ready, cudaStream_t s) {
+             bool rows_ready, cudaStream_t s) {
   if (T < 0 || K < 1 || K > MOE_MAX_TOPK || H < 8 || H % 8 != 0 || n_rows < 0)
     return MOE_ERR_INVALID_ARGUMENT;
   if (weights_dtype != MOE_DTYPE_F32 && weights_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARGUMENT;
@@ -223,7 +246,7 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
   if (st != MOE_OK) return st;
 
   FinArgs a{rows, (long long)n_rows, row_index, weights, shared, routed_scaling_factor, T, K, H, out, dev.error_word,
-            inputs_ready ? 0 : 1};
+            rows_ready ? 0 : 1};
   const bool gather = row_index != nullptr, bf16w = weights_dtype == MOE_DTYPE_BF16, sh = shared != nullptr;
   if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, dev.sm_count, s);
   if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, dev.sm_count, s);

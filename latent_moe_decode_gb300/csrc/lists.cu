@@ -16,16 +16,19 @@
 // walked in steps of 32 (lane l reads id step*32 + l: every load a coalesced 128
 // bytes; all steps of a part in flight at once -- one L2 round trip, since round trips,
 // not arithmetic, set this kernel's time). Pass 1 counts, per (warp, owned expert), the
-// matches (shared-memory atomics: counts do not depend on order) and, per lane, the ids
-// below the range; the owned slot of each loaded id (or "none") stays in registers, a
-// byte an id. Warp j scans expert j's counts over the warps (shuffles) into each warp's
-// start within the CTA's share. The CTAs then exchange their per-expert totals and
+// matches -- each step's matching lanes grouped by expert (__match_any_sync), the
+// group's lowest lane writing its size to a per-warp table, lane j summing expert j's
+// column, so every shared-memory cell has one writer and no atomic is used -- and, per
+// lane, the ids below the range; the owned slot of each loaded id (or "none") stays in
+// registers, a byte an id. Warp j scans expert j's counts over the warps (shuffles)
+// into each warp's start within the CTA's share. The CTAs then exchange their per-expert totals and
 // below-counts through distributed shared memory (after a cluster barrier), so each
 // knows where its share of every list starts, and CTA 0 writes the range's offsets.
 // Pass 2 places a block of 16 steps without a serial chain: the ranks inside every step
 // come from __match_any_sync at once (no step waits on another), a per-warp table turns
 // the steps' group sizes into per-step starts, and every match is then written in
-// parallel -- lists in ascending index order. No workspace, no global atomics.
+// parallel -- lists in ascending index order. No workspace and no atomics (shared or
+// global): the counts and placements come from warp votes and single-writer tables.
 #include "common.cuh"
 
 namespace moe {
@@ -56,9 +59,13 @@ struct Scan {
 };
 
 // Pass 1 over kBatch steps from flat id b0 (+ lane); CHECK also flags ids outside [0, E).
+// Within each step the lanes holding an owned expert are grouped by it
+// (__match_any_sync) and the group's lowest lane writes the group size to
+// tab[step][expert] -- one writer per cell, no atomics; lane j then adds column j (its
+// expert) to its count.
 template <bool CHECK, bool HOLD>
-__device__ __forceinline__ void count_batch(const ListArgs& a, Scan& sc, int b0, int r1, int lane, int* cnt,
-                                            int step0) {
+__device__ __forceinline__ void count_batch(const ListArgs& a, Scan& sc, int b0, int r1, int lane,
+                                            uint16_t (*tab)[kMaxEpc], int& count, int step0) {
   int v[kBatch];
 #pragma unroll
   for (int u = 0; u < kBatch; ++u) {
@@ -67,17 +74,27 @@ __device__ __forceinline__ void count_batch(const ListArgs& a, Scan& sc, int b0,
     if (CHECK && i < r1 && (unsigned)v[u] >= (unsigned)a.E) sc.bad = true;
   }
 #pragma unroll
+  for (int u = 0; u < kBatch; ++u) tab[u][lane] = 0;
+  __syncwarp();
+#pragma unroll
   for (int u = 0; u < kBatch; ++u) {
     sc.below += (unsigned)v[u] < (unsigned)sc.e_lo;
     const unsigned jv = (unsigned)(v[u] - sc.e_lo);
-    if (jv < (unsigned)sc.nexp) {
-      atomicAdd(&cnt[jv], 1);
+    const bool m = jv < (unsigned)sc.nexp;
+    const unsigned bal = __ballot_sync(kFull, m);
+    if (m) {
+      const unsigned peers = __match_any_sync(bal, jv);
+      if ((peers & ((1u << lane) - 1u)) == 0) tab[u][jv] = (uint16_t)__popc(peers);
       if (HOLD) {
         const int st = step0 + u;
         sc.held[st / 4] &= ~((~jv & 0xFFu) << (8 * (st % 4)));
       }
     }
   }
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) count += tab[u][lane];
+  __syncwarp();
 }
 
 // Pass 2 for one block of up to kBatch steps of a warp: the ids i0 + 32*st + lane, with
@@ -170,23 +187,24 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
   const int r0 = min(c1, c0 + warp * per), r1 = min(c1, r0 + per);
   static_assert(kMaxEpc == 32 && kWarps == 16, "one lane per owned expert; two expert columns per warp");
   static_assert(kHeld == kBatch && kBatch % 4 == 0, "held steps are one pass-2 block");
-  s_cnt[warp][lane] = 0;
-  __syncthreads();
 
   grid_wait();
   grid_launch_dependents();  // after the wait: dependents may rely on all before the lists
 
-  // pass 1
+  // pass 1: lane j counts this warp's matches of owned expert j
   int* cnt = s_cnt[warp];
+  uint16_t(*tab)[kMaxEpc] = s_tab[warp];
+  int count = 0;
   const bool check = blockIdx.y == 0;  // the first expert range's cluster checks every id once
   if (r0 < r1) {
-    if (check) count_batch<true, true>(a, sc, r0, r1, lane, cnt, 0);
-    else count_batch<false, true>(a, sc, r0, r1, lane, cnt, 0);
+    if (check) count_batch<true, true>(a, sc, r0, r1, lane, tab, count, 0);
+    else count_batch<false, true>(a, sc, r0, r1, lane, tab, count, 0);
   }
   for (int b0 = r0 + 32 * kHeld; b0 < r1; b0 += 32 * kBatch) {
-    if (check) count_batch<true, false>(a, sc, b0, r1, lane, cnt, 0);
-    else count_batch<false, false>(a, sc, b0, r1, lane, cnt, 0);
+    if (check) count_batch<true, false>(a, sc, b0, r1, lane, tab, count, 0);
+    else count_batch<false, false>(a, sc, b0, r1, lane, tab, count, 0);
   }
+  cnt[lane] = count;
   if (check && __any_sync(kFull, sc.bad) && lane == 0) set_error(a.err, MOE_DEVERR_EXPERT_ID);
   const int below = __reduce_add_sync(kFull, sc.below);
   if (lane == 0) s_below[warp] = below;
@@ -240,7 +258,6 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
     a.offsets[sc.e_lo + threadIdx.x] = s_base[threadIdx.x];
 
   // pass 2
-  uint16_t(*tab)[kMaxEpc] = s_tab[warp];
   if (r0 < r1) place_block(a, sc.held, r0, min(kBatch, (r1 - r0 + 31) / 32), sc.nexp, lane, tab, cnt, s_start);
   for (int b0 = r0 + 32 * kHeld; b0 < r1; b0 += 32 * kBatch) {
     uint32_t slot[kBatch / 4];

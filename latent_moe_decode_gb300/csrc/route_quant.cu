@@ -1,8 +1,7 @@
 // Sigmoid + bias top-K and MXFP8 quantisation of the latent rows in one launch.
 //
-// Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideRoute:
-// one launch of 2b CTAs in which CTA t routes token t and CTA b + t writes token t's
-// MXFP8 plan row from the BF16 latent.
+// Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideRoute
+// (the top-K CTAs and the latent-quantisation CTAs of a batch share one grid).
 //
 // GB300 design: the two jobs share nothing, so in one grid the quantisation CTAs
 // stream the latent through HBM on the SMs the routing CTAs leave free, instead of

@@ -52,6 +52,7 @@ extern "C" int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, f
                                          moe_stream_t stream) {
   using namespace moe;
   if (T < 1 || E < 1 || H < 8 || H % 8 != 0) return MOE_ERR_INVALID_ARGUMENT;
+  if ((long long)T * E > (1LL << 40)) return MOE_ERR_CAPACITY;  // as moe_router_logits
   if (!x || !w || !logits) return MOE_ERR_INVALID_ARGUMENT;
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(logits, 4)) return MOE_ERR_ALIGNMENT;
   DeviceInfo dev;

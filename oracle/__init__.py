@@ -93,8 +93,15 @@ def _c(a, dtype):
 
 
 # ---------------------------------------------------------------------------
-def router_logits(x: np.ndarray, w: np.ndarray):
-    """FP64 logits [T,E] and sum_j |x*w| [T,E] of BF16 x [T,H], W [E,H]."""
+_PARALLEL_MACS = 1 << 26  # inputs larger than this many multiply-adds use every host core
+
+
+def router_logits(x: np.ndarray, w: np.ndarray, threads: int | None = None):
+    """FP64 logits [T,E] and sum_j |x*w| [T,E] of BF16 x [T,H], W [E,H].
+
+    Every token's row is independent, so large inputs are cut into contiguous token
+    ranges, each computed by the same C function on its own host thread (ctypes
+    releases the GIL during the call); the per-element arithmetic is unchanged."""
     x = _c(x, np.uint16)
     w = _c(w, np.uint16)
     T, H = x.shape
@@ -102,7 +109,24 @@ def router_logits(x: np.ndarray, w: np.ndarray):
     assert w.shape[1] == H
     out = np.empty((T, E), np.float64)
     ab = np.empty((T, E), np.float64)
-    _load().oracle_router_logits(_ptr(x), _ptr(w), T, H, E, _ptr(out), _ptr(ab))
+    lib = _load()
+    if threads is None:
+        threads = (os.cpu_count() or 1) if T * E * H > _PARALLEL_MACS else 1
+    threads = max(1, min(int(threads), T))
+    if threads == 1:
+        lib.oracle_router_logits(_ptr(x), _ptr(w), T, H, E, _ptr(out), _ptr(ab))
+        return out, ab
+    from concurrent.futures import ThreadPoolExecutor
+
+    bounds = np.linspace(0, T, threads + 1).astype(int)
+
+    def part(i):
+        t0, t1 = int(bounds[i]), int(bounds[i + 1])
+        if t1 > t0:
+            lib.oracle_router_logits(_ptr(x[t0:t1]), _ptr(w), t1 - t0, H, E, _ptr(out[t0:t1]), _ptr(ab[t0:t1]))
+
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(part, range(threads)))
     return out, ab
 
 

@@ -1,7 +1,7 @@
 """The whole routing-and-combine step on one stream (router -> top-16 with the MXFP8
 latent in the same launch -> lists -> Finalize, programmatic dependent launches between
-the kernels) against the oracle, at the decode shapes: logits within tolerance, everything else bit for bit,
-with the oracle's top-k consuming the GPU's logits."""
+the kernels) against the oracle, at the decode shapes: every logit within tolerance, everything else bit for
+bit, with the oracle's top-k consuming the GPU's logits."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +12,7 @@ from gpu_helpers import bf16_bits, bf16_dev, dev, host
 pytestmark = pytest.mark.gpu
 
 
-def _check_chain(moe, orc, T, skew=False, samples=None, graph=False):
+def _check_chain(moe, orc, T, skew=False, graph=False):
     d = synth.chain_inputs(T, skew=skew)
     x, w, bias, latent, rows = bf16_dev(d["x"]), bf16_dev(d["w"]), dev(d["bias"]), bf16_dev(d["latent"]), bf16_dev(d["rows"])
     rf = moe.RouteFinalize(T, synth.H, synth.L, synth.E, synth.K)
@@ -32,15 +32,11 @@ def _check_chain(moe, orc, T, skew=False, samples=None, graph=False):
     torch.cuda.synchronize()
     assert moe.device_error(clear=True) == 0
     logits = host(rf.logits)
-    # R1 logits, sampled or full, against FP64
-    if samples:
-        rng = np.random.default_rng(T)
-        t, e = rng.integers(0, T, samples).astype(np.int32), rng.integers(0, synth.E, samples).astype(np.int32)
-        exp, ab = orc.router_logits_sampled(d["x"], d["w"], t, e)
-        assert np.all(np.abs(logits[t, e].astype(np.float64) - exp) <= 1e-5 * ab)
-    else:
-        exp, ab = orc.router_logits(d["x"], d["w"])
-        assert np.all(np.abs(logits.astype(np.float64) - exp) <= 1e-5 * ab)
+    # R1: every logit against FP64 (the oracle splits the tokens over the host cores)
+    exp, ab = orc.router_logits(d["x"], d["w"])
+    err = np.abs(logits.astype(np.float64) - exp)
+    bad = np.argwhere(err > 1e-5 * ab)
+    assert bad.size == 0, f"{len(bad)} logits out of tolerance, first at (t, e) = {tuple(bad[0])}"
     # R2 top-16 from the GPU's logits
     ids, wf, wb = orc.topk_route(logits, d["bias"], synth.K)
     np.testing.assert_array_equal(host(rf.ids), ids)
@@ -67,17 +63,17 @@ def test_narrow(moe, orc):
 
 
 def test_wide(moe, orc):
-    _check_chain(moe, orc, 1020, samples=4000)
+    _check_chain(moe, orc, 1020)
 
 
 @pytest.mark.parametrize("T", [1, 16, 64, 256, 1020, 4096])
 def test_skew_sweep(moe, orc, T):
     """The skew sweep's token counts, Zipf(1.1) expert popularity."""
-    _check_chain(moe, orc, T, skew=True, samples=None if T <= 16 else 3000)
+    _check_chain(moe, orc, T, skew=True)
 
 
 def test_wide_in_cuda_graph(moe, orc):
-    _check_chain(moe, orc, 1020, samples=2000, graph=True)
+    _check_chain(moe, orc, 1020, graph=True)
 
 
 @pytest.mark.parametrize("T", [1, 8, 64, 100, 256, 1020, 2048, 4096])

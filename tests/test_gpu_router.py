@@ -41,10 +41,24 @@ def test_random_within_tolerance(moe, orc, algo, T, E, H):
     assert np.all(np.abs(got - exp) <= 1e-5 * ab)
 
 
+@pytest.mark.parametrize("T", [1, 16, 64, 256, 1020, 2048, 4096])
+def test_full_size_every_element(moe, orc, T):
+    """The public call (its own plan at each T: 16-CTA clusters of narrow tiles, 64- and
+    128-column tiles, 5-CTA clusters of 256-column tiles at T = 1020, CTA pairs) at the
+    full decode shapes (896 x 7168 gate): every logit against FP64."""
+    x = synth.hidden_rows(T)
+    w = synth.router_weight()
+    got = host(moe.router_logits(bf16_dev(x), bf16_dev(w))).astype(np.float64)
+    exp, ab = orc.router_logits(x, w)
+    bad = np.argwhere(np.abs(got - exp) > 1e-5 * ab)
+    assert bad.size == 0, f"{len(bad)} logits out of tolerance, first at (t, e) = {tuple(bad[0])}"
+
+
 @pytest.mark.parametrize("algo", list(ALGOS))
 @pytest.mark.parametrize("T", [1020, 2048, 4096])
 def test_full_size_sampled(moe, orc, algo, T):
-    """The full decode shapes (896 x 7168 gate): 3000 sampled outputs against FP64."""
+    """Each kernel family forced at the full decode shapes: 3000 sampled outputs against
+    FP64 (a quick check; the public call is compared element by element above)."""
     x = synth.hidden_rows(T)
     w = synth.router_weight()
     got = host(moe.router_logits(bf16_dev(x), bf16_dev(w), algo=ALGOS[algo])).astype(np.float64)

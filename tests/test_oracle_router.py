@@ -39,3 +39,15 @@ def test_sampled_matches_full(orc):
     s, sab = orc.router_logits_sampled(x, w, t, e)
     np.testing.assert_array_equal(s, full[t, e])
     np.testing.assert_array_equal(sab, fab[t, e])
+
+
+def test_token_ranges_on_threads_match_one_call(orc):
+    """The threaded form (token ranges on host threads) gives the single call's values,
+    bit for bit, including ranges of uneven length."""
+    x = synth.normal_bf16(7, 1, (13, 384), 1.0)
+    w = synth.normal_bf16(7, 2, (29, 384), 0.02)
+    one, one_ab = orc.router_logits(x, w, threads=1)
+    for n in (2, 5, 13, 40):
+        par, par_ab = orc.router_logits(x, w, threads=n)
+        np.testing.assert_array_equal(par, one)
+        np.testing.assert_array_equal(par_ab, one_ab)

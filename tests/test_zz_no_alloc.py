@@ -4,9 +4,9 @@ the C ABI, against the regular moe_router_logits on the same inputs.
 It exists for callers that cannot allocate device memory when they compute the
 router logits (an engine whose memory pool owns the device after start-up, a plug-in
 given only its inputs and outputs): it keeps the split-K partials in an array the
-library reserves itself. Three calls in a row with different shapes check that what
-the previous call left in that shared array never leaks into a result. Kept in a file
-of its own, collected last."""
+library reserves itself. Calls in a row with different shapes check that what the
+previous call left in that shared array never leaks into a result. Kept in a file of
+its own, collected last."""
 import ctypes
 
 import numpy as np
@@ -31,9 +31,13 @@ def _noalloc(moe, x, w):
 
 
 def test_noalloc_matches_router_logits(moe):
-    torch.backends.cuda.matmul.allow_tf32 = False
+    """Calls in a row over every plan shape the router takes at the decode widths --
+    T = 1, 8, 16, 64 (narrow tiles, up to 16 splits in a cluster), 256 (128-column
+    tiles), 1020 (256-column tiles in 5-CTA clusters) -- each bit-identical to the
+    regular entry point, so nothing an earlier call left in the shared array leaks in."""
+    torch.backends.cuda.matmul.allow_tf32 = False  # the tolerance bound below in full FP32
     w = bf16_dev(synth.router_weight())
-    for T, seed in ((1020, 1), (256, 2), (1020, 3)):
+    for T, seed in ((1, 11), (8, 12), (64, 13), (1020, 14), (16, 15), (256, 16), (1020, 17)):
         x = bf16_dev(synth.hidden_rows(T, seed=seed))
         got = _noalloc(moe, x, w)
         ref = moe.router_logits(x, w)  # the regular entry point, caller-owned workspace
@@ -42,6 +46,17 @@ def test_noalloc_matches_router_logits(moe):
         assert torch.all((got - ref).abs() <= bound), f"T={T}"
         assert torch.equal(got, ref), f"T={T}: not bit-identical"
     assert moe.device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("T", [1, 16, 64, 256, 1020, 4096])
+def test_noalloc_fits_every_decode_width(moe, T):
+    """With the 896 x 7168 gate the array holds the partials of every token count the
+    decode step uses (the call returns OK, not MOE_ERR_CAPACITY)."""
+    w = bf16_dev(synth.router_weight())
+    x = bf16_dev(synth.hidden_rows(T, seed=20 + T))
+    got = _noalloc(moe, x, w)
+    torch.cuda.synchronize()
+    assert torch.equal(got, moe.router_logits(x, w)), f"T={T}"
 
 
 def test_noalloc_rejects_bad_arguments(moe):
@@ -54,3 +69,5 @@ def test_noalloc_rejects_bad_arguments(moe):
     assert lib.moe_router_logits_noalloc(p(x), p(w), p(out), 0, 64, 16, s) == moe.ERR_INVALID_ARGUMENT
     assert lib.moe_router_logits_noalloc(p(x), p(w), p(out), 8, 63, 16, s) == moe.ERR_INVALID_ARGUMENT
     assert lib.moe_router_logits_noalloc(ctypes.c_void_p(x.data_ptr() + 2), p(w), p(out), 8, 64, 16, s) == moe.ERR_ALIGNMENT
+    # T * E above 2^40 is refused before any plan or launch, as by moe_router_logits
+    assert lib.moe_router_logits_noalloc(p(x), p(w), p(out), 1 << 30, 64, 1 << 11, s) == moe.ERR_CAPACITY
