@@ -61,7 +61,7 @@ typedef struct CUstream_st* moe_stream_t;
 #define MOE_DTYPE_BF16 1
 
 /* Limits. */
-#define MOE_MAX_EXPERTS 1024 /* E of moe_topk_route and moe_build_routing_lists */
+#define MOE_MAX_EXPERTS 4096 /* E of moe_topk_route, moe_build_routing_lists and moe_build_unit_windows */
 #define MOE_MAX_TOPK 32      /* K of every call */
 
 /* Human-readable name of a status code (static string, never NULL). */

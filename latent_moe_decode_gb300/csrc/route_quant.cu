@@ -5,13 +5,14 @@
 //
 // GB300 design: the two jobs share nothing, so in one grid the quantisation CTAs
 // stream the latent through HBM on the SMs the routing CTAs leave free, instead of
-// running after them. T CTAs run the top-K selection of one token each (topk.cuh) and
-// Q CTAs each quantise a 16 KB span of the latent (mxfp8.cuh), one bulk copy per CTA.
-// Inside moe_route_finalize the latent is an input of the whole step, so the
-// quantisation CTAs need not wait for the router (the router signals its dependents
-// only after its own wait): they come first in the grid and run on the SMs the router
-// leaves idle. Both bodies are the ones the separate calls use, so the results are
-// identical to moe_topk_route followed by mxfp8_quantize_rows.
+// running after them. The routing CTAs run the top-K selection (topk.cuh: four tokens
+// per CTA, one per warp, at E <= 1024) and Q CTAs each quantise a 16 KB span of the
+// latent (mxfp8.cuh), one bulk copy per CTA. Inside moe_route_finalize the latent is an
+// input of the whole step, so the quantisation CTAs need not wait for the router (the
+// router signals its dependents only after its own wait): they come first in the grid
+// and run on the SMs the router leaves idle. Both bodies are the ones the separate
+// calls use, so the results are identical to moe_topk_route followed by
+// mxfp8_quantize_rows.
 #include "mxfp8.cuh"
 #include "topk.cuh"
 
@@ -21,21 +22,21 @@ namespace {
 using namespace topk_impl;
 constexpr int kQuantUnroll = 8;  // 128 threads x 8 chunks = 16 KB per quantisation CTA
 
-template <int NJ, bool PART>
+template <int NJ, bool WARP, bool PART>
 __global__ void __launch_bounds__(kThreads) route_quant_kernel(const TopkArgs a, const uint16_t* __restrict__ x,
                                                                long long nchunks, uint8_t* __restrict__ q,
                                                                uint8_t* __restrict__ scales, uint32_t* err, int qblocks,
-                                                               int quant_wait) {
+                                                               int rblocks, int quant_wait) {
   // Blocks are dispatched in index order. When the quantisation CTAs need not wait they
   // come first and take the SMs that are free while the preceding kernel still runs;
   // otherwise the routing CTAs (the longer ones) come first.
   const int b = (int)blockIdx.x;
   if (quant_wait) {
-    if (b < a.T) topk_token<NJ, PART>(a, b);
-    else mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)(b - a.T), true);
+    if (b < rblocks) route_block<NJ, WARP, PART>(a, b);
+    else mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)(b - rblocks), true);
   } else {
     if (b < qblocks) mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)b, false);
-    else topk_token<NJ, PART>(a, b - qblocks);
+    else route_block<NJ, WARP, PART>(a, b - qblocks);
   }
 }
 
@@ -59,7 +60,9 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   const long long nchunks = (long long)rows * (cols / 8);
   const long long per = (long long)kThreads * kQuantUnroll;
   const long long qblocks = (nchunks + per - 1) / per;
-  if ((long long)T + qblocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
+  const bool warp = E <= kWarpMaxE;
+  const long long rblocks = route_blocks(T, warp);
+  if (rblocks + qblocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
@@ -71,25 +74,27 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
     a.logits_out = const_cast<float*>(logits);
     a.discard = (E % 32 == 0 && aligned(part, 128)) ? 1 : 0;
   }
-  const dim3 grid((unsigned)(T + qblocks)), block(kThreads);
-  const int qb = (int)qblocks, qw = latent_ready ? 0 : 1;
-  switch ((E + 127) / 128) {
-#define MOE_RQ_CASE(N)                                                                                     \
-  case N:                                                                                                   \
-    return part ? launch_pdl(route_quant_kernel<N, true>, grid, block, 0, s, a, latent, nchunks, q, scales,     \
-                             dev.error_word, qb, qw)                                                         \
-                : launch_pdl(route_quant_kernel<N, false>, grid, block, 0, s, a, latent, nchunks, q, scales,    \
-                             dev.error_word, qb, qw);
-    MOE_RQ_CASE(1)
-    MOE_RQ_CASE(2)
-    MOE_RQ_CASE(3)
-    MOE_RQ_CASE(4)
-    MOE_RQ_CASE(5)
-    MOE_RQ_CASE(6)
-    MOE_RQ_CASE(7)
-    MOE_RQ_CASE(8)
-#undef MOE_RQ_CASE
+  const dim3 grid((unsigned)(rblocks + qblocks)), block(kThreads);
+  const int qb = (int)qblocks, rb = (int)rblocks, qw = latent_ready ? 0 : 1;
+#define MOE_RQ_LAUNCH(NJ, W)                                                                                      \
+  return part ? launch_pdl(route_quant_kernel<NJ, W, true>, grid, block, 0, s, a, latent, nchunks, q, scales,     \
+                           dev.error_word, qb, rb, qw)                                                            \
+              : launch_pdl(route_quant_kernel<NJ, W, false>, grid, block, 0, s, a, latent, nchunks, q, scales,    \
+                           dev.error_word, qb, rb, qw);
+  if (!warp) {
+    MOE_RQ_LAUNCH(32, false)
   }
+  switch ((E + 127) / 128) {  // experts per lane, rounded up to a multiple of 4
+    case 1: MOE_RQ_LAUNCH(4, true)
+    case 2: MOE_RQ_LAUNCH(8, true)
+    case 3: MOE_RQ_LAUNCH(12, true)
+    case 4: MOE_RQ_LAUNCH(16, true)
+    case 5: MOE_RQ_LAUNCH(20, true)
+    case 6: MOE_RQ_LAUNCH(24, true)
+    case 7: MOE_RQ_LAUNCH(28, true)
+    case 8: MOE_RQ_LAUNCH(32, true)
+  }
+#undef MOE_RQ_LAUNCH
   return MOE_ERR_CAPACITY;
 }
 

@@ -8,21 +8,21 @@
 // Selection key c_e = sigmoid(logit_e) + bias_e; order (c descending, expert index
 // ascending); weights are the unbiased scores over their slot-order FP32 sum.
 //
-// GB300 design: one CTA of 4 warps per token. Thread i holds the experts i + 128 j
-// (j < NJ), so each load instruction of a warp reads 128 contiguous bytes of the
-// logits row. Selection runs in two tiers. Every expert first gets an approximate key
-// (the hardware's approximate exp2 and reciprocal: within 1.79e-7 of the specified
-// sigmoid over all inputs). The K-th largest of the 128 thread maxima is a lower bound
-// of the K-th largest key (K different threads hold a key at least that large): each
-// warp sorts its 32 maxima with a bitonic network over shuffles, and two rounds of
-// bitonic merging of the four sorted lists give the top 32 of all 128. Every expert
-// whose approximate key is within a margin of that bound (about 17 of 896 for random
-// scores) is a candidate -- the margin covers twice the approximation error, so the
-// exact top K are among them. Only the candidates get the specified sigmoid and their
-// exact keys; up to 32 are ranked by one warp (each lane counts the candidates whose
-// (key, ~expert) orders before its own: 32 independent comparisons), 32 < count <= 64
-// by counting over shared memory, more (heavy ties) by exact keys for all and K rounds
-// of argmax. The result is that of the exact keys, bit for bit.
+// GB300 design: one warp per token (E <= 1024; four tokens per CTA of 128 threads),
+// no CTA barrier. Lane l holds the experts l + 32 j (28 at E = 896), so each load
+// instruction of the warp reads one 128-byte line of the logits row. Selection runs in
+// two tiers. Every expert first gets an approximate key (1/2 + tanh(x/2)/2 with the
+// hardware's approximate tanh: one MUFU operation, within 2^-11 of the specified
+// sigmoid over all inputs). The K-th largest of the 32 lane maxima is a lower bound of
+// the K-th largest key (K different lanes hold a key at least that large), found by a
+// bitonic sort over shuffles. Every expert whose approximate key is within a margin of
+// that bound (about 23 of 896 for the decode batches) is a candidate -- the margin
+// covers twice the approximation error, so the exact top K are among them. Only the
+// candidates get the specified sigmoid and their exact keys; up to 64 are ranked by
+// shuffles (each candidate counts the candidates whose (key, ~expert) orders before its
+// own: independent comparisons), more (heavy ties) by exact keys for all and K rounds
+// of a warp argmax. The result is that of the exact keys, bit for bit. For 1024 < E
+// <= 4096 one CTA of 4 warps takes a token (topk.cuh).
 #include "topk.cuh"
 
 namespace moe {
@@ -30,9 +30,9 @@ namespace {
 
 using namespace topk_impl;
 
-template <int NJ>
+template <int NJ, bool WARP>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
-  topk_token<NJ>(a, blockIdx.x);
+  route_block<NJ, WARP, false>(a, blockIdx.x);
 }
 
 }  // namespace
@@ -55,17 +55,19 @@ extern "C" int moe_topk_route(const float* logits, const float* bias, int T, int
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
-  dim3 grid(T), block(kThreads);
+  const bool warp = E <= kWarpMaxE;
+  const dim3 grid((unsigned)route_blocks(T, warp)), block(kThreads);
   cudaStream_t s = as_cuda(stream);
-  switch ((E + 127) / 128) {
-    case 1: return launch_pdl(topk_kernel<1>, grid, block, 0, s, a);
-    case 2: return launch_pdl(topk_kernel<2>, grid, block, 0, s, a);
-    case 3: return launch_pdl(topk_kernel<3>, grid, block, 0, s, a);
-    case 4: return launch_pdl(topk_kernel<4>, grid, block, 0, s, a);
-    case 5: return launch_pdl(topk_kernel<5>, grid, block, 0, s, a);
-    case 6: return launch_pdl(topk_kernel<6>, grid, block, 0, s, a);
-    case 7: return launch_pdl(topk_kernel<7>, grid, block, 0, s, a);
-    case 8: return launch_pdl(topk_kernel<8>, grid, block, 0, s, a);
+  if (!warp) return launch_pdl(topk_kernel<32, false>, grid, block, 0, s, a);
+  switch ((E + 127) / 128) {  // experts per lane, rounded up to a multiple of 4
+    case 1: return launch_pdl(topk_kernel<4, true>, grid, block, 0, s, a);
+    case 2: return launch_pdl(topk_kernel<8, true>, grid, block, 0, s, a);
+    case 3: return launch_pdl(topk_kernel<12, true>, grid, block, 0, s, a);
+    case 4: return launch_pdl(topk_kernel<16, true>, grid, block, 0, s, a);
+    case 5: return launch_pdl(topk_kernel<20, true>, grid, block, 0, s, a);
+    case 6: return launch_pdl(topk_kernel<24, true>, grid, block, 0, s, a);
+    case 7: return launch_pdl(topk_kernel<28, true>, grid, block, 0, s, a);
+    case 8: return launch_pdl(topk_kernel<32, true>, grid, block, 0, s, a);
   }
   return MOE_ERR_CAPACITY;
 }

@@ -1,5 +1,7 @@
 // Sigmoid + bias top-K: the per-token selection shared by the top-K kernel and the
-// fused top-K + MXFP8 launch.
+// fused top-K + MXFP8 launch. Two bodies: one warp per token for E <= 1024 (the decode
+// shapes: 28 experts per lane at E = 896, no CTA barrier), and one CTA of 4 warps per
+// token for 1024 < E <= 4096.
 #pragma once
 
 #include "common.cuh"
@@ -58,16 +60,15 @@ __device__ __forceinline__ float spec_sigmoid(float x) {
   return hi ? 1.0f : (lo ? 0.0f : r);
 }
 
-// A fast sigmoid used only to find the candidates: 1 / (1 + 2^(-x log2 e)) with the
-// hardware's approximate exp2 and reciprocal. Over all 2^32 inputs it differs from
-// spec_sigmoid by at most 1.79e-7 (< 2^-22.4; measured exhaustively on the GPU and
-// pinned by a test) and agrees on NaN.
-constexpr float kApproxErr = 2.384185791e-7f;  // 2^-22: the bound the margin below assumes
+// A fast sigmoid used only to find the candidates: 1/2 + tanh(x/2)/2 with the
+// hardware's approximate tanh (one MUFU operation). Over all 2^32 inputs it stays
+// within kApproxErr of spec_sigmoid (measured exhaustively on the GPU and pinned by a
+// test) and agrees on NaN.
+constexpr float kApproxErr = 0x1p-11f;
 __device__ __forceinline__ float approx_sigmoid(float x) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(__fmul_rn(-x, kLog2e)));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, e)));
-  return r;
+  float th;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(__fmul_rn(0.5f, x)));
+  return __fmaf_rn(0.5f, th, 0.5f);
 }
 
 // Monotone 32-bit key of an FP32 value: larger value -> larger key, -0 == +0,
@@ -101,14 +102,252 @@ struct TopkArgs {
   int discard = 0;
 };
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 128;  // both bodies: CTAs of 4 warps
 constexpr int kWarps = kThreads / 32;
+constexpr int kWarpMaxE = 1024;  // the warp body's experts (32 per lane at most)
 
-// One token's selection, run by a CTA of kThreads threads. PART: the logits are summed
-// from the router's split-K partials (a.part) and written (a.logits_out); a separate
-// instantiation, so the plain selection keeps its register count (and occupancy).
+// The logits of this thread's experts e = e_first + e_stride * j (j < NJ; a warp's 32
+// lanes cover one 128-byte line per j). PART: the sum in split order of the router's S
+// partials (two splits' loads in flight at a time), written to a.logits_out, and the
+// lines read invalidated in L2 when a.discard is set (E % 32 == 0, aligned workspace).
+template <int NJ, bool PART>
+__device__ __forceinline__ void load_logits(const TopkArgs& a, int t, int e_first, int e_stride, float (&x)[NJ]) {
+  const int E = a.E;
+  if constexpr (PART) {
+    for (int s0 = 0; s0 < a.S; s0 += 2) {
+      const float* r0 = a.part + ((size_t)s0 * a.T + t) * E;
+      const float* r1 = r0 + (size_t)a.T * E;
+      const bool two = s0 + 1 < a.S;
+      float p0[NJ], p1[NJ];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int e = e_first + e_stride * j;
+        p0[j] = e < E ? __ldcg(r0 + e) : 0.f;
+        p1[j] = (two && e < E) ? __ldcg(r1 + e) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        x[j] = s0 == 0 ? p0[j] : __fadd_rn(x[j], p0[j]);
+        if (two) x[j] = __fadd_rn(x[j], p1[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = e_first + e_stride * j;
+      if (e < E) a.logits_out[(size_t)t * E + e] = x[j];
+    }
+    __syncwarp();  // every lane's loads are consumed before their lines are invalidated
+    if (a.discard) {
+      const int lane = threadIdx.x & 31, w0 = e_first - lane;  // the warp's first expert
+      for (int l = lane; l < a.S * NJ; l += 32) {
+        const int s = l / NJ, j = l - s * NJ;
+        const int e0 = w0 + e_stride * j;
+        if (e0 < E)
+          asm volatile("discard.global.L2 [%0], 128;" ::"l"(a.part + ((size_t)s * a.T + t) * E + e0) : "memory");
+      }
+    }
+  } else {
+    const float* lg = a.logits + (size_t)t * E;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = e_first + e_stride * j;
+      x[j] = e < E ? __ldg(lg + e) : 0.f;
+    }
+  }
+}
+
+// Descending bitonic sort of one value per lane over the warp (shuffles): lane l ends
+// with the (l+1)-th largest.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kFull, v, j);
+      const bool descending = (lane & k) == 0;
+      const bool keep_max = ((lane & j) == 0) == descending;
+      v = keep_max ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
+}
+
+// Candidate threshold from a bound on approximate keys. K experts have an approximate
+// key >= bound, so the exact K-th largest key is >= bound - err, and every exact
+// top-K expert has an approximate key >= bound - 2 err, where err (|approximate -
+// exact key|) is at most kApproxErr plus an ulp or two of the key. The margin
+// 2 kApproxErr + 2^-21 (1 + |bound|) covers that; a bound that is not a finite number
+// takes every expert.
+__device__ __forceinline__ uint32_t candidate_threshold(uint32_t bound) {
+  if (bound < 2u) return 1u;
+  const float f = key_value(bound);
+  const float g = __fsub_rn(f, 2.0f * kApproxErr + 0x1p-21f * (1.0f + fabsf(f)));
+  return isfinite(g) ? order_key(g) : 1u;
+}
+
+// (exact key << 32) | ~expert: one integer order for "key descending, expert ascending".
+__device__ __forceinline__ unsigned long long rank_key(uint32_t key, int e) {
+  return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)e);
+}
+
+// The exact key and score of an expert with logit xv and bias bv.
+__device__ __forceinline__ uint32_t exact_key(const TopkArgs& a, float xv, float bv, float* sc) {
+  const float sv = spec_sigmoid(xv);
+  *sc = sv;
+  return order_key(a.bias ? __fadd_rn(sv, bv) : sv);
+}
+
+// Outputs of token t from its slots (slot order): by lanes 0..K-1 of one warp. The
+// weights are the unbiased scores over their FP32 sum taken in slot order.
+__device__ __forceinline__ void write_slots(const TopkArgs& a, int t, const int32_t* slot_id, const float* slot_s) {
+  const int lane = threadIdx.x & 31;
+  if (lane >= a.K) return;
+  float S = 0.f;
+  for (int k = 0; k < a.K; ++k) S = __fadd_rn(S, slot_s[k]);
+  const float sv = slot_s[lane];
+  float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(sv, S)) : sv;
+  if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
+  const size_t o = (size_t)t * a.K + lane;
+  a.ids[o] = slot_id[lane];
+  if (a.weights) a.weights[o] = w;
+  if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
+}
+
+// ---------------------------------------------------------------------------------
+// One warp per token (E <= kWarpMaxE). Lane l holds the experts l + 32 j (each load
+// instruction of the warp reads one 128-byte line of the logits row).
+struct WarpScratch {
+  int32_t e[64];  // candidates: expert, logit, bias (at most 64 take the ranking paths)
+  float x[64];
+  float b[64];
+  int32_t slot_id[MOE_MAX_TOPK];
+  float slot_s[MOE_MAX_TOPK];
+};
+
+template <int NJ, bool PART>
+__device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, WarpScratch& ws) {
+  static_assert(NJ <= 32, "one flag bit per expert of a lane");
+  const int lane = threadIdx.x & 31;
+  const int E = a.E, K = a.K;
+  float x[NJ], b[NJ];
+  load_logits<NJ, PART>(a, t, lane, 32, x);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    b[j] = (a.bias && e < E) ? __ldg(a.bias + e) : 0.f;
+  }
+  // 1) approximate keys; the lane maximum
+  uint32_t key[NJ], m = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const float sv = approx_sigmoid(x[j]);
+    const float c = a.bias ? __fadd_rn(sv, b[j]) : sv;
+    key[j] = lane + 32 * j < E ? order_key(c) : 0u;
+    m = max(m, key[j]);
+  }
+  // 2) bound: the K-th largest of the 32 lane maxima (K different lanes hold a key at
+  //    least that large)
+  const uint32_t thr = candidate_threshold(__shfl_sync(kFull, warp_sort_desc(m), K - 1));
+  // 3) candidates: every expert at or above the threshold, counted and compacted in
+  //    lane order
+  uint32_t flags = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (key[j] >= thr && key[j] != 0u) flags |= 1u << j;
+  const int mine = __popc(flags);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int total = __shfl_sync(kFull, incl, 31);
+  if (total <= 64) {
+    int pos = incl - mine;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (flags & (1u << j)) {
+        ws.e[pos] = lane + 32 * j;
+        ws.x[pos] = x[j];
+        ws.b[pos] = b[j];
+        ++pos;
+      }
+    }
+    __syncwarp();
+    // 4) exact keys of the candidates (lane i: candidates i and i + 32); the slot of a
+    //    candidate is the number of candidates ordering before it (keys made distinct
+    //    by the expert in the low word): independent comparisons over shuffles
+    unsigned long long c0 = 0, c1 = 0;
+    float s0 = 0.f, s1 = 0.f;
+    if (lane < total) c0 = rank_key(exact_key(a, ws.x[lane], ws.b[lane], &s0), ws.e[lane]);
+    if (lane + 32 < total) c1 = rank_key(exact_key(a, ws.x[lane + 32], ws.b[lane + 32], &s1), ws.e[lane + 32]);
+    int r0 = 0, r1 = 0;
+    if (total <= 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r0 += __shfl_sync(kFull, c0, i) > c0;
+    } else {
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const unsigned long long o0 = __shfl_sync(kFull, c0, i), o1 = __shfl_sync(kFull, c1, i);
+        r0 += (o0 > c0) + (o1 > c0);
+        r1 += (o0 > c1) + (o1 > c1);
+      }
+    }
+    if (lane < total && r0 < K) {
+      ws.slot_id[r0] = (int32_t)(0xFFFFFFFFu - (uint32_t)c0);
+      ws.slot_s[r0] = s0;
+    }
+    if (lane + 32 < total && r1 < K) {
+      ws.slot_id[r1] = (int32_t)(0xFFFFFFFFu - (uint32_t)c1);
+      ws.slot_s[r1] = s1;
+    }
+  } else {
+    // heavy ties (more than 64 candidates): exact keys of all experts, then K rounds of
+    // a warp argmax over (key descending, expert ascending)
+    float sc[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const uint32_t kx = exact_key(a, x[j], b[j], &sc[j]);
+      key[j] = lane + 32 * j < E ? kx : 0u;
+    }
+    for (int k = 0; k < K; ++k) {
+      uint32_t bk = 0;
+      int be = 0x7FFFFFFF;
+      float bs = 0.f;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        if (key[j] > bk) {  // ascending expert order within the lane: the first maximum wins
+          bk = key[j];
+          be = lane + 32 * j;
+          bs = sc[j];
+        }
+      }
+      const uint32_t wk = __reduce_max_sync(kFull, bk);
+      const int we = (int)__reduce_min_sync(kFull, bk == wk ? (uint32_t)be : 0x7FFFFFFFu);
+      const float wsv = __shfl_sync(kFull, bs, we & 31);  // expert e lives in lane e % 32
+      if (lane == 0) {
+        ws.slot_id[k] = we;
+        ws.slot_s[k] = wsv;
+      }
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        if (lane + 32 * j == we) key[j] = 0u;
+    }
+  }
+  __syncwarp();
+  // 5) weights
+  write_slots(a, t, ws.slot_id, ws.slot_s);
+}
+
+// ---------------------------------------------------------------------------------
+// One CTA of kThreads threads per token (kWarpMaxE < E <= 32 * kThreads). Thread i
+// holds the experts i + 128 j. The bound is the K-th largest of the 128 thread maxima
+// (each warp sorts its 32, two rounds of bitonic merges give the top 32 of all 128);
+// up to 32 candidates are ranked by warp 0 over shuffles, up to 64 by counting over
+// shared memory, more (heavy ties) by exact keys for all and K rounds of argmax.
 template <int NJ, bool PART = false>
-__device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
+__device__ __forceinline__ void topk_token_cta(const TopkArgs& a, const int t) {
   __shared__ uint32_t s_top[kWarps][32];
   __shared__ int s_cnt[kWarps];
   __shared__ uint32_t l_key[kListCap];
@@ -121,52 +360,11 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
   __shared__ float r_s[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, K = a.K;
-  grid_launch_dependents();
-  grid_wait();
-  const float* lg = a.logits + (size_t)t * E;
 
   // 1) approximate keys of this thread's experts tid + 128 j
   uint32_t key[NJ];
   float x[NJ], b[NJ];
-  if constexpr (PART) {
-    // the logits: the S partials summed in split order, 4 splits' loads in flight at once
-    constexpr int kSG = 4;
-    for (int s0 = 0; s0 < a.S; s0 += kSG) {
-      float p[kSG][NJ];
-#pragma unroll
-      for (int i = 0; i < kSG; ++i)
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const int e = tid + 128 * j;
-          p[i][j] = (s0 + i < a.S && e < E) ? __ldcg(a.part + ((size_t)(s0 + i) * a.T + t) * E + e) : 0.f;
-        }
-#pragma unroll
-      for (int i = 0; i < kSG; ++i)
-        if (s0 + i < a.S)
-#pragma unroll
-          for (int j = 0; j < NJ; ++j) x[j] = s0 + i == 0 ? p[i][j] : __fadd_rn(x[j], p[i][j]);
-    }
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int e = tid + 128 * j;
-      if (e < E) a.logits_out[(size_t)t * E + e] = x[j];
-    }
-    __syncwarp();  // every lane's loads are consumed before their lines are invalidated
-    if (a.discard) {  // whole 128-byte lines of this warp's experts (E % 32 == 0, aligned)
-      for (int l = lane; l < a.S * NJ; l += 32) {
-        const int s = l / NJ, j = l - s * NJ;
-        const int e0 = 32 * warp + 128 * j;
-        if (e0 < E)
-          asm volatile("discard.global.L2 [%0], 128;" ::"l"(a.part + ((size_t)s * a.T + t) * E + e0) : "memory");
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int e = tid + 128 * j;
-      x[j] = e < E ? __ldg(lg + e) : 0.f;
-    }
-  }
+  load_logits<NJ, PART>(a, t, tid, 128, x);
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int e = tid + 128 * j;
@@ -183,18 +381,7 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
   }
 
   // 2) bound: the K-th largest of the 128 thread maxima
-  uint32_t v = tmax;
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint32_t o = __shfl_xor_sync(kFull, v, j);
-      const bool descending = (lane & k) == 0;
-      const bool keep_max = ((lane & j) == 0) == descending;
-      v = keep_max ? max(v, o) : min(v, o);
-    }
-  }
-  s_top[warp][lane] = v;  // descending: lane l holds the warp's (l+1)-th largest
+  s_top[warp][lane] = warp_sort_desc(tmax);  // descending: lane l holds the warp's (l+1)-th largest
   __syncthreads();
   // top 32 of the union of two descending lists: max(a[l], b[31-l]) is bitonic;
   // five half-cleaner steps sort it descending
@@ -210,18 +397,7 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
   const uint32_t m01 = merge(s_top[0][lane], s_top[1][31 - lane]);
   const uint32_t m23 = merge(s_top[2][lane], s_top[3][31 - lane]);
   const uint32_t top = merge(m01, __shfl_sync(kFull, m23, 31 - lane));
-  const uint32_t bound = __shfl_sync(kFull, top, K - 1);
-  // K experts (one in each of K threads) have an approximate key >= bound, so the exact
-  // K-th largest key is >= bound - err, and every exact top-K expert has an approximate
-  // key >= bound - 2 err, err = |approximate - exact key| <= 2^-22 + a few ulps of the
-  // key. The margin 2^-19 (1 + |bound|) covers that; a bound that is not a finite
-  // number takes every expert.
-  uint32_t thr = 1u;
-  if (bound >= 2u) {
-    const float f = key_value(bound);
-    const float g = __fsub_rn(f, 0x1p-19f * (1.0f + fabsf(f)));
-    if (isfinite(g)) thr = order_key(g);
-  }
+  const uint32_t thr = candidate_threshold(__shfl_sync(kFull, top, K - 1));
 
   // 3) candidates at or above the threshold, compacted in thread order
   uint32_t flags = 0;
@@ -244,15 +420,8 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
     total += s_cnt[w];
   }
 
-  // exact key and score of candidate expert e (logit xv, bias bv)
-  auto exact = [&](float xv, float bv, float* sc) {
-    const float sv = spec_sigmoid(xv);
-    *sc = sv;
-    return order_key(a.bias ? __fadd_rn(sv, bv) : sv);
-  };
   if (total <= 32) {
-    // compact, then one warp computes the exact keys and sorts (key desc, expert asc):
-    // lane k holds slot k
+    // compact, then one warp computes the exact keys and ranks them
     int pos = before + incl - mine;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
@@ -265,14 +434,9 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
     }
     __syncthreads();
     if (warp != 0) return;
-    unsigned long long c = 0;  // (key << 32) | ~expert; 0 = empty
+    unsigned long long c = 0;  // rank_key; 0 = empty
     float cs = 0.f;
-    if (lane < total) {
-      const uint32_t k = exact(l_s[lane], __uint_as_float(l_key[lane]), &cs);
-      c = ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)l_e[lane]);
-    }
-    // slot of each candidate = how many candidates order before it (keys distinct with the
-    // expert in the low word): 32 independent comparisons instead of a sorting network
+    if (lane < total) c = rank_key(exact_key(a, l_s[lane], __uint_as_float(l_key[lane]), &cs), l_e[lane]);
     int rank = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) rank += __shfl_sync(kFull, c, j) > c;
@@ -281,24 +445,7 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
       slot_s[rank] = cs;
     }
     __syncwarp();
-    // weights: unbiased scores over their slot-order FP32 sum (all loads first, then the
-    // sum in order)
-    float sc[MOE_MAX_TOPK];
-#pragma unroll
-    for (int k = 0; k < MOE_MAX_TOPK; ++k) sc[k] = k < K ? slot_s[k] : 0.f;
-    float S = 0.f;
-#pragma unroll
-    for (int k = 0; k < MOE_MAX_TOPK; ++k)
-      if (k < K) S = __fadd_rn(S, sc[k]);
-    if (lane < K) {
-      const float sv = slot_s[lane];
-      float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(sv, S)) : sv;
-      if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
-      const size_t o = (size_t)t * K + lane;
-      a.ids[o] = slot_id[lane];
-      if (a.weights) a.weights[o] = w;
-      if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
-    }
+    write_slots(a, t, slot_id, slot_s);
     return;
   }
   if (total <= kListCap) {
@@ -307,7 +454,7 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
     for (int j = 0; j < NJ; ++j) {
       if (flags & (1u << j)) {
         float sc;
-        l_key[pos] = exact(x[j], b[j], &sc);
+        l_key[pos] = exact_key(a, x[j], b[j], &sc);
         l_e[pos] = tid + 128 * j;
         l_s[pos] = sc;
         ++pos;
@@ -333,7 +480,7 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
     float s[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const uint32_t kx = exact(x[j], b[j], &s[j]);
+      const uint32_t kx = exact_key(a, x[j], b[j], &s[j]);
       key[j] = tid + 128 * j < E ? kx : 0u;
     }
     for (int k = 0; k < K; ++k) {
@@ -379,20 +526,27 @@ __device__ __forceinline__ void topk_token(const TopkArgs& a, const int t) {
     }
   }
   __syncthreads();
+  if (warp == 0) write_slots(a, t, slot_id, slot_s);
+}
 
-  // 4) weights: unbiased scores over their slot-order FP32 sum
-  if (tid < K) {
-    float S = 0.f;
-    for (int k = 0; k < K; ++k) S = __fadd_rn(S, slot_s[k]);
-    const float sv = slot_s[tid];
-    float w = a.renorm ? (S == 0.f ? 0.f : __fdiv_rn(sv, S)) : sv;
-    if (a.scale != 1.0f) w = __fmul_rn(w, a.scale);
-    const size_t o = (size_t)t * K + tid;
-    a.ids[o] = slot_id[tid];
-    if (a.weights) a.weights[o] = w;
-    if (a.weights_bf16) a.weights_bf16[o] = f32_to_bf16(w);
+// The routing part of a launch: CTA `blk` of the routing CTAs. Warp body (E <=
+// kWarpMaxE): its 4 warps take tokens 4 blk .. 4 blk + 3; CTA body: token blk. Waits for
+// the preceding kernel (which writes the logits or partials) before reading.
+template <int NJ, bool WARP, bool PART>
+__device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
+  grid_launch_dependents();
+  grid_wait();
+  if constexpr (WARP) {
+    __shared__ WarpScratch ws[kWarps];
+    const int warp = threadIdx.x >> 5, t = blk * kWarps + warp;
+    if (t < a.T) topk_token_warp<NJ, PART>(a, t, ws[warp]);
+  } else {
+    topk_token_cta<NJ, PART>(a, blk);
   }
 }
+
+// Routing CTAs for T tokens.
+__host__ __device__ constexpr int route_blocks(int T, bool warp) { return warp ? (T + kWarps - 1) / kWarps : T; }
 
 }  // namespace topk_impl
 }  // namespace moe

@@ -10,35 +10,42 @@
 // min(offsets[e] + (j+1)W, offsets[e+1]). Units are numbered by expert, then j;
 // unit_offsets is the exclusive prefix sum of the per-expert unit counts.
 //
-// GB300 design: one CTA of 1024 threads (E <= 1024 experts, one per thread) reads the
-// offsets (at most 4 KB), scans the unit counts (warp shuffles, then one warp over the
-// 32 warp totals), and then every thread writes units u = tid, tid + 1024, ... (each
-// finds its expert by binary search over the scanned counts in shared memory), so the
-// writes are coalesced and a heavy expert's units are spread over all threads.
+// GB300 design: one CTA of 1024 threads (E <= 4096 experts, up to four consecutive
+// experts per thread) reads the offsets (at most 16 KB), scans the unit counts (each
+// thread's own experts, warp shuffles, then one warp over the 32 warp totals), and then
+// every thread writes units u = tid, tid + 1024, ... (each finds its expert by binary
+// search over the scanned counts in shared memory), so the writes are coalesced and a
+// heavy expert's units are spread over all threads.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kPer = MOE_MAX_EXPERTS / kThreads;  // experts per thread
 
 __global__ void __launch_bounds__(kThreads, 1)
     units_kernel(const int32_t* __restrict__ offsets, int E, int W, int32_t* __restrict__ unit_offsets,
                  int32_t* __restrict__ unit_expert, int32_t* __restrict__ unit_start, int32_t* __restrict__ unit_len,
                  int max_units, uint32_t* err) {
-  __shared__ int32_t uoff[kThreads + 1];  // exclusive unit prefix per expert
-  __shared__ int32_t woff[kThreads + 1];  // list offsets
+  __shared__ int32_t uoff[MOE_MAX_EXPERTS + 1];  // exclusive unit prefix per expert
+  __shared__ int32_t woff[MOE_MAX_EXPERTS + 1];  // list offsets
   __shared__ int32_t wsum[32];
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   grid_wait();
   grid_launch_dependents();
-  int n = 0, o = 0;
-  if (e < E) {
-    o = offsets[e];
-    n = offsets[e + 1] - o;
+  // this thread's experts e0 .. e0 + kPer - 1 (those below E)
+  const int e0 = tid * kPer;
+  int o[kPer + 1], u[kPer], mine = 0;
+#pragma unroll
+  for (int i = 0; i <= kPer; ++i) o[i] = e0 + i <= E ? offsets[e0 + i] : 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int n = e0 + i < E ? o[i + 1] - o[i] : 0;
+    u[i] = n > 0 ? (n + W - 1) / W : 0;
+    mine += u[i];
   }
-  const int u = n > 0 ? (n + W - 1) / W : 0;
-  int incl = u;  // inclusive scan within the warp
+  int incl = mine;  // inclusive scan of the thread totals within the warp
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
@@ -56,22 +63,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     wsum[lane] = sc - v;  // exclusive over warps
   }
   __syncthreads();
-  const int excl = wsum[warp] + incl - u;
-  if (e < E) {
-    uoff[e] = excl;
-    woff[e] = o;
-  }
-  if (e == E - 1) {  // (thread E - 1 alone writes entry E)
-    uoff[E] = excl + u;
-    woff[E] = o + n;
+  int excl = wsum[warp] + incl - mine;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      uoff[e] = excl;
+      woff[e] = o[i];
+      excl += u[i];
+      if (e == E - 1) {  // (the thread holding expert E - 1 alone writes entry E)
+        uoff[E] = excl;
+        woff[E] = o[i + 1];
+      }
+    }
   }
   __syncthreads();
-  if (e < E) unit_offsets[e] = uoff[e];
-  if (e == 0) unit_offsets[E] = uoff[E];
+  for (int e = tid; e <= E; e += kThreads) unit_offsets[e] = uoff[e];
   const int total = uoff[E];
-  if (e == 0 && total > max_units) set_error(err, MOE_DEVERR_CAPACITY);  // not within the capacity bound
+  if (tid == 0 && total > max_units) set_error(err, MOE_DEVERR_CAPACITY);  // not within the capacity bound
   const int lim = total < max_units ? total : max_units;
-  for (int i = e; i < lim; i += kThreads) {
+  for (int i = tid; i < lim; i += kThreads) {
     int lo = 0, hi = E - 1;  // the expert x with uoff[x] <= i < uoff[x + 1]
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;

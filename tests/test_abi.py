@@ -68,7 +68,7 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.moe_finalize(A16, 64, None, A16, 0, None, 1.0, 0, 16, 3584, A16, None) == 0  # T = 0: no-op
     assert lib.moe_topk_route(A16, None, 4, 896, 0, 1, 1.0, A16, None, None, None) == 1
     assert lib.moe_topk_route(A16, None, 4, 16, 17, 1, 1.0, A16, None, None, None) == 1
-    assert lib.moe_topk_route(A16, None, 4, 2048, 16, 1, 1.0, A16, None, None, None) == 3
+    assert lib.moe_topk_route(A16, None, 4, 4097, 16, 1, 1.0, A16, None, None, None) == 3
     assert lib.moe_topk_route(A16, None, 4, 896, 33, 1, 1.0, A16, None, None, None) == 3
     assert lib.mxfp8_quantize_rows(A16, 4, 33, A16, A16, None) == 1
     assert lib.mxfp8_quantize_rows(A16, 4, 0, A16, A16, None) == 1
@@ -76,7 +76,7 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.mxfp8_quantize_rows_ex(A16, 4, 64, A16, A16, 2, None) == 1
     assert lib.mxfp8_quantize_rows_ex(A16, 4, 33, A16, A16, 1, None) == 1
     assert lib.moe_build_routing_lists(A16, 4, 0, 896, A16, A16, None, 0, None) == 1
-    assert lib.moe_build_routing_lists(A16, 4, 16, 1025, A16, A16, None, 0, None) == 3
+    assert lib.moe_build_routing_lists(A16, 4, 16, 4097, A16, A16, None, 0, None) == 3
     assert lib.moe_router_logits_ex(A16, A16, A16, 0, 7168, 896, None, 0, 0, None) == 1
     assert lib.moe_router_logits_ex(A16, A16, A16, 8, 7167, 896, None, 0, 0, None) == 1
     assert lib.moe_router_logits_ex(A16, A16, A16, 8, 7168, 896, None, 0, 7, None) == 1
@@ -92,7 +92,7 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.moe_router_logits_ex(P(264), A16, A16, 8, 7168, 896, None, 0, 0, None) == 2
     assert lib.moe_build_unit_windows(A16, 0, 8, A16, A16, A16, A16, 4, None) == 1
     assert lib.moe_build_unit_windows(A16, 896, 0, A16, A16, A16, A16, 4, None) == 1
-    assert lib.moe_build_unit_windows(A16, 1025, 8, A16, A16, A16, A16, 4, None) == 3
+    assert lib.moe_build_unit_windows(A16, 4097, 8, A16, A16, A16, A16, 4, None) == 3
     assert lib.moe_build_unit_windows(A16, 896, 8, A16, None, A16, A16, 4, None) == 1
     assert lib.moe_build_unit_windows(P(258), 896, 8, A16, A16, A16, A16, 4, None) == 2
     assert lib.moe_unit_windows_capacity(1020, 16, 896, 8) == 2040 + 896
