@@ -168,13 +168,19 @@ class Step:
                 with torch.cuda.graph(g):
                     self.run_direct(i)
                 self.graphs.append(g)
-            self.chain_graph, self.chain = None, chain
+            self.chain_graph, self.warm_graph, self.chain = None, None, chain
             if chain > 1:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
                     for i in range(chain):
                         self.run_direct(i)
                 self.chain_graph = g
+                # the same number of consecutive steps, all on the first input set (no rotation)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(chain):
+                        self.run_direct(0)
+                self.warm_graph = g
 
     def run_direct(self, i=0):
         st = self.sets[i % self.nsets]
@@ -310,6 +316,68 @@ def rotations(step, K):
     return {k: [v[i % len(v)] for i in range(K)] for k, v in rot.items()}, {"router": nr, "topk+mxfp8": nq, "finalize": nf}
 
 
+def shared_bytes(d):
+    """Algorithmic bytes of Finalize with the shared expert: the rows not skipped (index
+    -1) read once, indices, weights and shared rows read once, the output written once."""
+    T, K, H = d["T"], d["K"], d["H"]
+    live = int(np.count_nonzero(d["row_index"] != -1))
+    return live * H * 2 + T * K * 4 + T * K * 2 + T * H * 2 + T * H * 2
+
+
+def time_finalize_shared(dev, steps, warmup):
+    """Finalize with the shared expert at its own workload (T=512, K=8, H=7168, 5 % -1
+    indices, routed scale 2.5, shared row), launches back to back over enough input
+    copies that every launch reads cold inputs."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    d = synth.finalize_shared_inputs()
+    T, K = d["T"], d["K"]
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    by = shared_bytes(d)
+    n = n_copies(by)
+    rows = [bf(d["rows"]) for _ in range(n)]
+    shared = [bf(d["shared"]) for _ in range(n)]
+    idx = torch.from_numpy(d["row_index"]).to(dev)
+    w = bf(d["weights"])
+    out = torch.empty(T, d["H"], dtype=torch.bfloat16, device=dev)
+    calls = [lambda i=i: m.finalize(rows[i % n], w, T, K, row_index=idx, shared=shared[i % n], scale=d["scale"], out=out)
+             for i in range(steps)]
+    for c in calls[: max(warmup, n)]:
+        c()
+    ms = time_back_to_back(calls, torch.cuda.current_stream())
+    hbm = load_peaks()[0]
+    gbs = by / (ms * 1e-3) / 1e9
+    del rows, shared
+    torch.cuda.empty_cache()
+    return {"workload": "Finalize with shared expert: T=512, K=8, H=7168, routed rows [4096,7168] gathered by "
+                        "permuted indices with 5 % -1, BF16 weights, routed_scaling_factor 2.5, shared rows [512,7168]",
+            "us": round(ms * 1e3, 2), "alg_bytes": by, "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
+            "timing": f"{steps} launches back to back over {n} input copies (cold inputs every launch)"}
+
+
+def percentiles(v):
+    v = np.asarray(v, dtype=np.float64)
+    return {"p10": round(float(np.percentile(v, 10)), 5), "p50": round(float(np.percentile(v, 50)), 5),
+            "p90": round(float(np.percentile(v, 90)), 5), "n": int(v.size)}
+
+
+def time_replays(g, n, stream, per):
+    """CUDA-event time of each of n consecutive replays of graph g, in ms per step
+    (a replay holds `per` steps)."""
+    import torch
+
+    torch.cuda._sleep(SLEEP_CYCLES)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        g.replay()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) / per for i in range(n)]
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -354,7 +422,15 @@ def run_ours(args, rank, world, local_rank):
         per_ms = {k: time_back_to_back(fns, stream) for k, fns in rot.items()}
         # (c) for reference: one step at a time, L2 flushed before each (outside events)
         flushed_ms = float(np.mean(time_region(step.run, args.steps, flush, stream)))
+        # (d) spread: each replay of a 12-step graph timed on its own (cold inputs), and the
+        #     same with every step on one input set (no rotation: what stays in L2 helps)
+        spread = time_replays(step.chain_graph, 15, stream, STEPS_PER_GRAPH)
+        for _ in range(2):
+            step.warm_graph.replay()
+        warm = time_replays(step.warm_graph, 15, stream, STEPS_PER_GRAPH)
     clocks = clk.summary()
+    assert m.device_error(clear=True) == 0
+    shared_line = time_finalize_shared(dev, args.steps, args.warmup)
     assert m.device_error(clear=True) == 0
 
     # (c) end to end through the public API: every step copies its inputs in from pinned
@@ -448,10 +524,15 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "chain_GB/s": round(chain_bytes(ab) / (ms * 1e-3) / 1e9, 1),
         "ms_per_step_flushed": round(flushed_ms, 5),
+        "ms_per_step_spread": dict(percentiles(spread), method="15 replays of a 12-step graph, each timed on its own "
+                                   "with CUDA events; cold inputs (rotation over the input copies)"),
+        "ms_per_step_warm": dict(percentiles(warm), method="the same with all 12 steps on one input set: the second "
+                                 "step onwards finds what L2 kept of the first (170 MB per step > 129 MB L2)"),
         "roofline": {"kernel": "finalize", "bound": "hbm", "achieved": round(fin_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(fin_gbs / hbm, 3), "traffic": traffic, "alg_bytes_per_launch": ab["finalize"],
                      "peak_source": f"{peak_src}: copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"},
         "steps_alone": steps,
+        "finalize_shared": shared_line,
         "e2e": {"value": round(whole_job_rate(T, world, e2e_ms), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "method": "moe_route_finalize per step; inputs in from pinned host memory and all results out, every "
@@ -464,29 +545,29 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_sweep(args):
-    """The skew sweep: the whole step per T with Zipf(1.1) expert popularity, plus each
-    call alone and the stock router; one JSON line per T."""
+def sweep_lines(Ts, args, skew=True, label="skew sweep"):
+    """The whole step per T (Zipf(1.1) expert popularity with skew, else the uniform
+    correction bias), plus each call alone and the stock router; one JSON line per T."""
     import torch
 
     import latent_moe_decode_gb300 as m
 
     dev = torch.device("cuda", 0)
     m.load()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     hbm = load_peaks()[0]
-    for T in [int(t) for t in args.sweep.split(",")]:
+    for T in Ts:
         for algo in ([0] if not args.router_algos else [int(a) for a in args.router_algos.split(",")]):
             ab = algorithmic_bytes(T)
             nsets = n_copies(chain_bytes(ab))
-            step = Step(T, dev, skew=True, router_algo=algo, nsets=nsets)
+            step = Step(T, dev, skew=skew, router_algo=algo, nsets=nsets)
             for i in range(args.warmup * nsets):
                 step.run(i)
             # K steps back to back over input copies larger than L2, as the main line
             ms = time_back_to_back([lambda i=i: step.run(i) for i in range(args.steps)], stream)
             rot, _ = rotations(step, args.steps)
             per = {k: round(time_back_to_back(fns, stream) * 1e3, 2) for k, fns in rot.items()}
+            frac = {k: round(ab[k] / (v * 1e-6) / 1e9 / hbm, 3) for k, v in per.items()}
             stock = None
             try:  # the stock router call (cuBLAS through torch), timed the same way, for context
                 nr = n_copies(ab["router"])
@@ -501,16 +582,34 @@ def run_sweep(args):
             except Exception:
                 pass
             loads = np.bincount(step.rf.ids.cpu().numpy().ravel(), minlength=synth.E)
-            print(json.dumps({"T": T, "router_algo": algo, "us_per_step": round(ms * 1e3, 2),
+            print(json.dumps({"config": label, "T": T, "router_algo": algo, "us_per_step": round(ms * 1e3, 2),
                               "tokens/s": round(T / (ms * 1e-3), 1), "chain_GB/s": round(chain_bytes(ab) / (ms * 1e-3) / 1e9, 1),
                               "frac_hbm_chain": round(chain_bytes(ab) / (ms * 1e-3) / 1e9 / hbm, 3), "us_alone": per,
-                              "us_stock_router_torch_mm": stock,
+                              "frac_hbm_alone": frac, "us_stock_router_torch_mm": stock,
                               "expert_load_max_over_mean": round(float(loads.max() / max(loads.mean(), 1e-9)), 2),
                               "timing": "back to back over input copies larger than L2 (cold inputs every launch)"}),
                   flush=True)
             assert m.device_error(clear=True) == 0
             del step, rot
             torch.cuda.empty_cache()
+
+
+def run_sweep(args):
+    sweep_lines([int(t) for t in args.sweep.split(",")], args)
+
+
+def run_configs(args):
+    """Every workload of the path, one JSON line each: tiny (T = 8), narrow (64) and wide
+    (1020) decode steps, Finalize with the shared expert (T = 512, K = 8, H = 7168), and
+    the Zipf(1.1) skew sweep (T = 1, 16, 64, 256, 1020, 4096)."""
+    import torch
+
+    for T, name in ((8, "tiny"), (64, "narrow"), (1020, "wide")):
+        sweep_lines([T], args, skew=False, label=name)
+    print(json.dumps(dict(config="finalize with shared expert", **time_finalize_shared(torch.device("cuda", 0),
+                                                                                        args.steps, args.warmup))),
+          flush=True)
+    sweep_lines([1, 16, 64, 256, 1020, 4096], args, skew=True)
 
 
 def front_flops_bytes(T, H=synth.H, E=synth.E, L=synth.L):
@@ -701,49 +800,108 @@ def run_ncu_front(args):
 
 
 # ---------------------------------------------------------------------------
+ORACLE_STEPS = ("router", "topk", "lists", "mxfp8", "finalize")
+REF_TOKENS = 16  # tokens per reference-arm step (a fixed slice of the wide batch)
+
+
 def oracle_step(d, tokens):
-    """The oracle's whole step over the given token rows of the wide batch."""
+    """The oracle's whole step over the given token rows of the wide batch, single
+    threaded; returns each step's seconds."""
     import oracle
 
-    x = d["x"][tokens]
-    logits, _ = oracle.router_logits(x, d["w"])
-    ids, wf, wb = oracle.topk_route(logits.astype(np.float32), d["bias"], synth.K)
-    oracle.routing_lists(ids, synth.E)
-    oracle.mxfp8_quantize(d["latent"][tokens])
+    clk, t = time.perf_counter, {}
+    x, lat = d["x"][tokens], d["latent"][tokens]
     rows = d["rows"].reshape(T_WIDE, synth.K, synth.L)[tokens].reshape(-1, synth.L)
+    t0 = clk()
+    logits, _ = oracle.router_logits(x, d["w"], threads=1)
+    t["router"] = clk() - t0
+    logits = logits.astype(np.float32)
+    t0 = clk()
+    ids, wf, wb = oracle.topk_route(logits, d["bias"], synth.K)
+    t["topk"] = clk() - t0
+    t0 = clk()
+    oracle.routing_lists(ids, synth.E)
+    t["lists"] = clk() - t0
+    t0 = clk()
+    oracle.mxfp8_quantize(lat)
+    t["mxfp8"] = clk() - t0
+    t0 = clk()
     oracle.finalize(rows, wb, len(tokens), synth.K)
+    t["finalize"] = clk() - t0
+    return t
+
+
+class OneCore:
+    """Pins this process to one host core for the oracle's timings (restored on exit)."""
+
+    def __enter__(self):
+        self.saved = None
+        try:
+            self.saved = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {min(self.saved)})
+        except (AttributeError, OSError):
+            pass
+        return self
+
+    def __exit__(self, *a):
+        if self.saved:
+            os.sched_setaffinity(0, self.saved)
 
 
 def cpu_baseline(seconds):
-    """The oracle as it stands, single-threaded on a host core, on consecutive 16-token
-    slices of the wide batch until about `seconds` of CPU work."""
+    """The oracle as it stands, single-threaded and pinned to one host core, on a
+    consecutive slice of the wide batch sized to about `seconds` of CPU work over three
+    passes; each step's time is the median of the three."""
     import oracle
 
     oracle.build()
     d = synth.chain_inputs(T_WIDE)
-    n, t0 = 0, time.perf_counter()
-    while time.perf_counter() - t0 < seconds and n < T_WIDE:
-        oracle_step(d, np.arange(n, min(n + 16, T_WIDE)))
-        n = min(n + 16, T_WIDE)
-    dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} of the {T_WIDE} tokens of the wide batch, whole step, {dt:.1f} s"}
+    with OneCore():
+        probe = sum(oracle_step(d, np.arange(4)).values()) / 4
+        n = int(min(T_WIDE, max(4, seconds / 3 / max(probe, 1e-6))))
+        tok = np.arange(n)
+        runs = [oracle_step(d, tok) for _ in range(3)]
+    per = {k: float(np.median([r[k] for r in runs])) for k in ORACLE_STEPS}
+    total = float(np.median([sum(r.values()) for r in runs]))
+    return {"value": round(n / total, 2), "unit": "tokens/s", "cores": 1, "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"tokens 0..{n - 1} of the {T_WIDE}-token wide batch, whole step, three passes "
+                      f"({3 * total:.1f} s), pinned to one core",
+            "per_step_ms": {k: round(v * 1e3, 2) for k, v in per.items()},
+            "per_step_us_per_token": {k: round(v * 1e6 / n, 1) for k, v in per.items()}}
 
 
 def run_reference(args, rank):
+    """The reference arm: the oracle (the plain C reference of the path), pinned to one
+    host core; every step is the whole routing-and-combine step over a fixed slice of
+    REF_TOKENS tokens of the wide batch. W untimed steps, then K timed steps."""
     if rank != 0:
         return None
-    tot = 0.0
-    for _ in range(args.warmup):
-        pass  # the oracle has no caches to warm beyond its first call below
-    base = cpu_baseline(max(2.0, args.cpu_seconds / max(1, args.steps)) * args.steps)
-    v = base["value"]
-    tot = T_WIDE / v
+    import oracle
+
+    oracle.build()
+    d = synth.chain_inputs(T_WIDE)
+    tok = np.arange(REF_TOKENS)
+    with OneCore():
+        for _ in range(args.warmup):
+            oracle_step(d, tok)
+        runs = []
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            runs.append(oracle_step(d, tok))
+        wall = time.perf_counter() - t0
+    ms = wall / args.steps * 1e3
+    v = round(REF_TOKENS / (wall / args.steps), 2)
+    base = {"value": v, "unit": "tokens/s", "cores": 1, "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"each step: tokens 0..{REF_TOKENS - 1} of the {T_WIDE}-token wide batch, whole step "
+                      f"(router, top-16, lists, MXFP8, Finalize), pinned to one core",
+            "per_step_ms": {k: round(float(np.median([r[k] for r in runs])) * 1e3, 3) for k in ORACLE_STEPS}}
     return {
         "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(tot * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 router / f32 rest", "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": WORKLOAD, "T": T_WIDE},
+        "config": {"workload": WORKLOAD, "T": T_WIDE, "hidden": synth.H, "latent": synth.L, "experts": synth.E,
+                   "top_k": synth.K, "parallelism": "one host core (rank 0 only)",
+                   "sample": f"{REF_TOKENS} tokens per step"},
         "cpu_baseline": base,
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -759,6 +917,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None, help="comma-separated T list: the skew sweep, one JSON line per T")
+    ap.add_argument("--configs", action="store_true", help="every workload (tiny, narrow, wide, Finalize with shared "
+                    "expert, skew sweep), one JSON line each")
     ap.add_argument("--router-algos", default=None, help="with --sweep: router kernel families to time (0 auto, 1 simt, 2 tcgen05)")
     ap.add_argument("--ncu-step", action="store_true", help="run the step untimed (for profiler captures)")
     ap.add_argument("--front", default=None, help="comma-separated T list: time the front projection, one JSON line per T")
@@ -798,6 +958,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     if args.impl == "reference":
         line = run_reference(args, rank)

@@ -300,6 +300,23 @@ int mxfp8_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* q, uint8
 int mxfp8_quantize_rows_ex(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales, int scale_rule,
                            moe_stream_t stream);
 
+/* The same quantisation with the scales laid out for a block-scaled tensor-core
+ * consumer: the tile layout that tcgen05.mma kind::mxf8f6f4 (one E8M0 scale per 32
+ * elements) reads through tcgen05.cp, as the PTX ISA describes it. The [rows, cols/32]
+ * scale matrix is cut into tiles of 128 rows x 4 scale columns, rows padded to a
+ * multiple of 128 and scale columns to a multiple of 4; tile (i, j) is the 512 bytes
+ * at (i * ceil(cols/128) + j) * 512, and inside it the scale of row r (0..127) and
+ * column c (0..3) is byte 16 * (r mod 32) + 4 * (r div 32) + c. Padding bytes are 0.
+ * Source: [wide] WideRoute (the token's plan row written with the swizzled plan_xsf
+ * scale layout the grouped expert GEMM reads; that layout itself is not shown, so this
+ * call offers the tensor cores' own layout); [ep] module docstring (the MXFP8 latent).
+ *   scales  device, mxfp8_tcgen05_scales_bytes(rows, cols) bytes, 16-byte aligned
+ * q, scale_rule, requirements and numerics as mxfp8_quantize_rows_ex; every scale byte
+ * equals the row-major call's. mxfp8_tcgen05_scales_bytes returns 0 for invalid sizes. */
+size_t mxfp8_tcgen05_scales_bytes(int rows, int cols);
+int mxfp8_quantize_rows_tcgen05(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales, int scale_rule,
+                                moe_stream_t stream);
+
 /* -------------------------------------------------------------------------------
  * Finalize: the routing-weighted top-K sum, optionally with the shared expert.
  * Source: [wide] Finalize (out[t] = sum_k w[t,k] * rows[16t + k], FP32, k in order,

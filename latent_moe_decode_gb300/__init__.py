@@ -20,7 +20,7 @@ __all__ = [
     "MoeError", "load", "router_logits", "router_logits_workspace", "front_projection",
     "front_projection_workspace", "topk_route",
     "build_routing_lists", "build_routing_lists_workspace", "unit_windows", "unit_windows_capacity",
-    "mxfp8_quantize_rows",
+    "mxfp8_quantize_rows", "mxfp8_quantize_rows_tcgen05", "mxfp8_tcgen05_scales_bytes",
     "finalize", "finalize_rmsnorm", "route_finalize", "route_finalize_workspace", "device_error", "RouteFinalize",
     "ROUTER_AUTO", "ROUTER_SIMT", "ROUTER_TCGEN05", "MXFP8_SCALE_FLOOR", "MXFP8_SCALE_CEIL",
     "DEVERR_ROW_INDEX", "DEVERR_EXPERT_ID", "DEVERR_TIMEOUT", "DEVERR_CAPACITY",
@@ -52,6 +52,8 @@ SIGNATURES = {
     "moe_build_unit_windows": (_I, [_P, _I, _I, _P, _P, _P, _P, _I, _P]),
     "mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "mxfp8_quantize_rows_ex": (_I, [_P, _I, _I, _P, _P, _I, _P]),
+    "mxfp8_tcgen05_scales_bytes": (_SZ, [_I, _I]),
+    "mxfp8_quantize_rows_tcgen05": (_I, [_P, _I, _I, _P, _P, _I, _P]),
     "moe_finalize": (_I, [_P, ctypes.c_int64, _P, _P, _I, _P, _F, _I, _I, _I, _P, _P]),
     "moe_finalize_rmsnorm": (_I, [_P, ctypes.c_int64, _P, _P, _I, _F, _P, _F, _I, _I, _I, _P, _P, _P]),
     "moe_route_finalize_workspace": (_SZ, [_I, _I, _I, _I]),
@@ -262,6 +264,24 @@ def mxfp8_quantize_rows(x, q=None, scales=None, stream=None, scale_rule: int = M
     scales = _empty((rows, nb), torch.uint8, x) if scales is None else _need(scales, torch.uint8, (rows, nb), "scales")
     _check("mxfp8_quantize_rows_ex", load().mxfp8_quantize_rows_ex(_ptr(x), rows, cols, _ptr(q), _ptr(scales),
                                                                    int(scale_rule), _stream(stream)))
+    return q, scales
+
+
+def mxfp8_tcgen05_scales_bytes(rows: int, cols: int) -> int:
+    """Bytes of the tcgen05 block-scaling scale layout of a [rows, cols] MXFP8 tensor."""
+    return int(load().mxfp8_tcgen05_scales_bytes(rows, cols))
+
+
+def mxfp8_quantize_rows_tcgen05(x, q=None, scales=None, stream=None, scale_rule: int = MXFP8_SCALE_FLOOR):
+    """(E4M3 bytes uint8 [rows, cols], E8M0 scales uint8 [mxfp8_tcgen05_scales_bytes]
+    in the tcgen05 block-scaling tile layout)."""
+    rows, cols = x.shape
+    _need(x, torch.bfloat16, (rows, cols), "x")
+    q = _empty((rows, cols), torch.uint8, x) if q is None else _need(q, torch.uint8, (rows, cols), "q")
+    n = mxfp8_tcgen05_scales_bytes(rows, cols)
+    scales = _empty((n,), torch.uint8, x) if scales is None else _need(scales, torch.uint8, (n,), "scales")
+    _check("mxfp8_quantize_rows_tcgen05", load().mxfp8_quantize_rows_tcgen05(
+        _ptr(x), rows, cols, _ptr(q), _ptr(scales), int(scale_rule), _stream(stream)))
     return q, scales
 
 

@@ -13,20 +13,19 @@
 // fragment) so that a warp covers 512 contiguous bytes of each row. The grid is
 // persistent (as many CTAs as fit: three per SM at K = 16) and thread i of the grid
 // takes the fragments i, i + G, i + 2G, ... (G threads in the grid). Each thread runs
-// its own ring of kStages shared-memory stages, each holding one item's K row
-// fragments, copied asynchronously (16-byte cp.async, bypassing L1, evict-first in
-// L2), and the item's K weights in registers. It waits for the oldest stage, sums it
-// (FP32 fma chain in k order, one 16-byte store) and refills that stage with the item
-// kStages ahead, so HBM always has kStages items of every thread in flight and the
-// stream does not drain between waves of CTAs; the weights, loaded one item ahead,
-// never add their latency to an item. Slots are private to their thread ([stage][k]
+// its own ring of kStages shared-memory stages: it issues the asynchronous 16-byte
+// copies (cp.async, bypassing L1, evict-first in L2) of all K row fragments of the
+// next item, and loads that item's K weights into registers, before it waits for and
+// sums the current one (FP32 fma chain in k order, one 16-byte store). HBM thus always
+// has the next items in flight and the stream does not drain between waves of CTAs;
+// the weights, loaded one item ahead, never add their latency to an item. Slots are private to their thread ([stage][k]
 // [thread]: conflict-free), so no CTA barrier is needed. Two stages and three CTAs per
 // SM keep more bytes in flight than three stages and two CTAs (the shared memory of
 // an SM holds six items either way).
 // When the rows are an input complete before the preceding kernel started (the
-// one-call step: the preceding kernels make only the weights), the first kStages
-// items' row copies are issued before griddepcontrol.wait and their weights are read
-// after it, so the first 30 MB of rows stream in while the preceding kernel finishes.
+// one-call step: the preceding kernels make only the weights), the first two items'
+// row copies are issued before griddepcontrol.wait and their weights are read after
+// it, so the first 30 MB of rows stream in while the preceding kernel finishes.
 #include "common.cuh"
 #include <type_traits>
 
@@ -84,8 +83,11 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   const uint32_t stage_bytes = (uint32_t)SL * kThreads * 16u;
 
   // Copies of fragment fi's K row fragments (and its shared-row fragment) into stage
-  // st, as one commit group (empty past the end); returns the mask of rows not skipped.
-  auto issue_rows = [&](int st, long long fi) -> uint32_t {
+  // st, as one commit group (empty past the end), and, with weights, its K raw weights
+  // into wraw[st]; returns the mask of rows not skipped.
+  using WRaw = typename std::conditional<BF16W, uint16_t, float>::type;
+  WRaw wraw[kStages][KM];
+  auto issue = [&](int st, long long fi, bool weights) -> uint32_t {
     uint32_t m = 0;
     if (fi < total) {
       const int t = (int)(fi / frags);
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
             set_error(a.err, MOE_DEVERR_ROW_INDEX);
             r = -1;
           }
+          if (weights) wraw[st][k] = __ldg(static_cast<const WRaw*>(a.weights) + ix);
           if (r != -1) {
             m |= 1u << k;
             cp_async16(base + (uint32_t)st * stage_bytes + (uint32_t)(k * kThreads * 16), a.rows + (size_t)r * H + col,
@@ -112,9 +115,6 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     cp_async_commit();
     return m;
   };
-  // fragment fi's K raw weights into wraw[st] (read one item ahead of their use)
-  using WRaw = typename std::conditional<BF16W, uint16_t, float>::type;
-  WRaw wraw[kStages][KM];
   auto load_weights = [&](int st, long long fi) {
     if (fi < total) {
       const int t = (int)(fi / frags);
@@ -124,23 +124,33 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     }
   };
 
-  // the first kStages items: rows first (before the wait when they are a step input),
-  // weights after the wait
+  // Each iteration issues the item one ahead, then waits for and sums the current one.
+  // When the rows are ready early, the first two items' rows are issued before the
+  // wait (the first iteration then issues nothing) and their weights read after it.
   uint32_t mask[kStages];
-#pragma unroll
-  for (int s = 0; s < kStages; ++s) mask[s] = issue_rows(s, f0 + s * stride);
-  if (early) grid_wait();  // the weights may come from the preceding kernel
-#pragma unroll
-  for (int s = 0; s < kStages; ++s) load_weights(s, f0 + s * stride);
-
+  static_assert(kStages == 2, "the early prologue issues exactly the first two items");
+  if (early) {
+    mask[0] = issue(0, f0, false);
+    mask[1] = issue(1, f0 + stride, false);
+    grid_wait();  // the weights may come from the preceding kernel
+    load_weights(0, f0);
+    load_weights(1, f0 + stride);
+  } else {
+    mask[0] = issue(0, f0, true);
+  }
+  bool ahead = early;  // the item one ahead is already issued
   for (long long f = f0; f < total; f += kStages * stride) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       const long long fi = f + s * stride;
+      constexpr int kAhead = kStages - 1;
+      const int sn = (s + kAhead) % kStages;
+      if (!ahead) mask[sn] = issue(sn, fi + kAhead * stride, true);
+      ahead = false;
       if (fi >= total) break;
       const int t = (int)(fi / frags);
       const int col = (int)(fi - (long long)t * frags) * 8;
-      // the weights, loaded one item ahead, times routed_scaling_factor
+      // the weights, loaded at issue, times routed_scaling_factor
       float w[KM];
 #pragma unroll
       for (int k = 0; k < KM; ++k) {
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
         }
         w[k] = wk;
       }
-      cp_async_wait<kStages - 1>();  // stage s has landed (the groups after it may not have)
+      cp_async_wait<kAhead>();
       // FP32 fma over k in order
       float acc[8];
 #pragma unroll
@@ -177,11 +187,6 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
           acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(q4[q]));
         }
       }
-      // stage s is consumed (its values are in registers): refill it with the item
-      // kStages ahead, so kStages items stay in flight
-      const long long fn = fi + kStages * stride;
-      mask[s] = issue_rows(s, fn);
-      load_weights(s, fn);
       uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);
       o.y = pack_bf16x2(acc[2], acc[3]);

@@ -15,14 +15,23 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Byte offset of scale (row r, scale column c) in the tcgen05 block-scaling layout:
+// 128 x 4 tiles of 512 bytes in row-tile-major order (ct column tiles per row tile);
+// inside a tile, 32 lines of 16 bytes, line l holding rows l, l + 32, l + 64, l + 96.
+__device__ __forceinline__ size_t tcgen05_scale_offset(int r, int c, int ct) {
+  return ((size_t)(r >> 7) * ct + (size_t)(c >> 2)) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (c & 3);
+}
+
 // One CTA's 16-byte chunks [block * THREADS * UNROLL, ...) of the flat input. With
 // wait = false the CTA does not wait for the preceding kernel (the caller knows the
 // input was complete before that kernel started). CEIL: the round-up scale rule (the
-// smallest power of two X with amax / X <= 448) instead of the OCP floor rule.
-template <int THREADS, int UNROLL, bool CEIL = false>
+// smallest power of two X with amax / X <= 448) instead of the OCP floor rule. TILED:
+// scales in the tcgen05 tile layout (nsc scale columns per row, ct column tiles)
+// instead of row-major.
+template <int THREADS, int UNROLL, bool CEIL = false, bool TILED = false>
 __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long long nchunks, uint8_t* __restrict__ q,
                                             uint8_t* __restrict__ scales, uint32_t* err, long long block,
-                                            bool wait = true) {
+                                            bool wait = true, int nsc = 0, int ct = 0) {
   constexpr int kThreads = THREADS, kUnroll = UNROLL;
   __shared__ __align__(128) uint4 stage[kThreads * kUnroll];
   __shared__ __align__(8) uint64_t bar_mem;
@@ -82,6 +91,15 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
     }
     const long long c = cta0 + cl;
     if (cl < nch) *reinterpret_cast<uint2*>(q + c * 8) = codes;
+    if constexpr (TILED) {
+      // the first lane of each block writes its scale byte at its tile position
+      if ((lane & 3) == 0 && cl < nch) {
+        const long long blk = c >> 2;  // = row * nsc + scale column
+        const int r = (int)(blk / nsc);
+        scales[tcgen05_scale_offset(r, (int)(blk - (long long)r * nsc), ct)] = (uint8_t)sbyte;
+      }
+      continue;
+    }
     // scale bytes of the warp's 8 blocks (held by lanes 0, 4, ..., 28)
     uint32_t b[8];
 #pragma unroll
@@ -98,6 +116,27 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
           if (i < nb) scales[blk0 + i] = (uint8_t)b[i];
       }
     }
+  }
+}
+
+// The padding bytes of the tcgen05 scale layout (rows past `rows` up to the row
+// tile, scale columns past nsc up to the column tile) set to 0, by every thread of
+// the grid in turn.
+__device__ __forceinline__ void tcgen05_scale_padding(uint8_t* __restrict__ scales, int rows, int nsc, int ct) {
+  const int cw = 4 * ct, rt_rows = (rows + 127) / 128 * 128;
+  const long long colpad = (long long)rows * (cw - nsc);
+  const long long total = colpad + (long long)(rt_rows - rows) * cw;
+  for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < total; p += (long long)gridDim.x * blockDim.x) {
+    int r, c;
+    if (p < colpad) {
+      r = (int)(p / (cw - nsc));
+      c = nsc + (int)(p - (long long)r * (cw - nsc));
+    } else {
+      const long long q2 = p - colpad;
+      r = rows + (int)(q2 / cw);
+      c = (int)(q2 - (long long)(r - rows) * cw);
+    }
+    scales[tcgen05_scale_offset(r, c, ct)] = 0;
   }
 }
 

@@ -60,7 +60,8 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   const long long nchunks = (long long)rows * (cols / 8);
   const long long per = (long long)kThreads * kQuantUnroll;
   const long long qblocks = (nchunks + per - 1) / per;
-  const bool warp = E <= kWarpMaxE;
+  // (with partials, the warp body also stores the logits as float4)
+  const bool warp = use_warp_body(T, E, part ? static_cast<const void*>(part) : logits, bias) && (!part || aligned(logits, 16));
   const long long rblocks = route_blocks(T, warp);
   if (rblocks + qblocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
   DeviceInfo dev;
@@ -81,18 +82,26 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
                            dev.error_word, qb, rb, qw)                                                            \
               : launch_pdl(route_quant_kernel<NJ, W, false>, grid, block, 0, s, a, latent, nchunks, q, scales,    \
                            dev.error_word, qb, rb, qw);
-  if (!warp) {
+  if (E > kWarpMaxE) {
     MOE_RQ_LAUNCH(32, false)
   }
-  switch ((E + 127) / 128) {  // experts per lane, rounded up to a multiple of 4
-    case 1: MOE_RQ_LAUNCH(4, true)
-    case 2: MOE_RQ_LAUNCH(8, true)
-    case 3: MOE_RQ_LAUNCH(12, true)
-    case 4: MOE_RQ_LAUNCH(16, true)
-    case 5: MOE_RQ_LAUNCH(20, true)
-    case 6: MOE_RQ_LAUNCH(24, true)
-    case 7: MOE_RQ_LAUNCH(28, true)
-    case 8: MOE_RQ_LAUNCH(32, true)
+  switch ((E + 127) / 128) {  // experts per thread (CTA body) or per lane / 4 (warp body)
+#define MOE_RQ_CASE(N)          \
+  case N:                       \
+    if (warp) {                 \
+      MOE_RQ_LAUNCH(N, true)    \
+    } else {                    \
+      MOE_RQ_LAUNCH(N, false)   \
+    }
+    MOE_RQ_CASE(1)
+    MOE_RQ_CASE(2)
+    MOE_RQ_CASE(3)
+    MOE_RQ_CASE(4)
+    MOE_RQ_CASE(5)
+    MOE_RQ_CASE(6)
+    MOE_RQ_CASE(7)
+    MOE_RQ_CASE(8)
+#undef MOE_RQ_CASE
   }
 #undef MOE_RQ_LAUNCH
   return MOE_ERR_CAPACITY;

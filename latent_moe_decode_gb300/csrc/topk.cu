@@ -55,19 +55,22 @@ extern "C" int moe_topk_route(const float* logits, const float* bias, int T, int
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
-  const bool warp = E <= kWarpMaxE;
+  const bool warp = use_warp_body(T, E, logits, bias);
   const dim3 grid((unsigned)route_blocks(T, warp)), block(kThreads);
   cudaStream_t s = as_cuda(stream);
-  if (!warp) return launch_pdl(topk_kernel<32, false>, grid, block, 0, s, a);
-  switch ((E + 127) / 128) {  // experts per lane, rounded up to a multiple of 4
-    case 1: return launch_pdl(topk_kernel<4, true>, grid, block, 0, s, a);
-    case 2: return launch_pdl(topk_kernel<8, true>, grid, block, 0, s, a);
-    case 3: return launch_pdl(topk_kernel<12, true>, grid, block, 0, s, a);
-    case 4: return launch_pdl(topk_kernel<16, true>, grid, block, 0, s, a);
-    case 5: return launch_pdl(topk_kernel<20, true>, grid, block, 0, s, a);
-    case 6: return launch_pdl(topk_kernel<24, true>, grid, block, 0, s, a);
-    case 7: return launch_pdl(topk_kernel<28, true>, grid, block, 0, s, a);
-    case 8: return launch_pdl(topk_kernel<32, true>, grid, block, 0, s, a);
+  if (E > kWarpMaxE) return launch_pdl(topk_kernel<32, false>, grid, block, 0, s, a);
+  switch ((E + 127) / 128) {  // experts per thread (CTA body) or per lane / 4 (warp body)
+#define MOE_TOPK_CASE(N) \
+  case N: return warp ? launch_pdl(topk_kernel<N, true>, grid, block, 0, s, a) : launch_pdl(topk_kernel<N, false>, grid, block, 0, s, a);
+    MOE_TOPK_CASE(1)
+    MOE_TOPK_CASE(2)
+    MOE_TOPK_CASE(3)
+    MOE_TOPK_CASE(4)
+    MOE_TOPK_CASE(5)
+    MOE_TOPK_CASE(6)
+    MOE_TOPK_CASE(7)
+    MOE_TOPK_CASE(8)
+#undef MOE_TOPK_CASE
   }
   return MOE_ERR_CAPACITY;
 }

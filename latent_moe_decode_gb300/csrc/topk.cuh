@@ -215,46 +215,120 @@ __device__ __forceinline__ void write_slots(const TopkArgs& a, int t, const int3
 }
 
 // ---------------------------------------------------------------------------------
-// One warp per token (E <= kWarpMaxE). Lane l holds the experts l + 32 j (each load
-// instruction of the warp reads one 128-byte line of the logits row).
+// One warp per token (E <= kWarpMaxE, E % 4 == 0, 16-byte aligned rows). Lane l holds
+// the experts 128 j + 4 l + i (j < NJ4, i < 4): one 16-byte load per j, so a load
+// instruction of the warp reads 512 contiguous bytes of the logits row.
 struct WarpScratch {
-  int32_t e[64];  // candidates: expert, logit, bias (at most 64 take the ranking paths)
-  float x[64];
-  float b[64];
+  float x[kWarpMaxE];  // the token's logits (exact keys of the candidates read them here)
+  int32_t e[64];       // candidates (at most 64 take the ranking paths)
   int32_t slot_id[MOE_MAX_TOPK];
   float slot_s[MOE_MAX_TOPK];
 };
 
-template <int NJ, bool PART>
+// The token's logits in the float4 layout (PART: summed from the split-K partials in
+// split order, two splits' loads in flight, written to a.logits_out, the lines read
+// invalidated in L2 when a.discard is set).
+template <int NJ4, bool PART>
+__device__ __forceinline__ void load_logits4(const TopkArgs& a, int t, float4 (&x)[NJ4]) {
+  const int lane = threadIdx.x & 31, E = a.E;
+  if constexpr (PART) {
+    for (int s0 = 0; s0 < a.S; s0 += 2) {
+      const float* r0 = a.part + ((size_t)s0 * a.T + t) * E;
+      const float* r1 = r0 + (size_t)a.T * E;
+      const bool two = s0 + 1 < a.S;
+      float4 p0[NJ4], p1[NJ4];
+#pragma unroll
+      for (int j = 0; j < NJ4; ++j) {
+        const int e = 128 * j + 4 * lane;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        p0[j] = e < E ? __ldcg(reinterpret_cast<const float4*>(r0 + e)) : z;
+        p1[j] = (two && e < E) ? __ldcg(reinterpret_cast<const float4*>(r1 + e)) : z;
+      }
+#pragma unroll
+      for (int j = 0; j < NJ4; ++j) {
+        if (s0 == 0) {
+          x[j] = p0[j];
+        } else {
+          x[j].x = __fadd_rn(x[j].x, p0[j].x), x[j].y = __fadd_rn(x[j].y, p0[j].y);
+          x[j].z = __fadd_rn(x[j].z, p0[j].z), x[j].w = __fadd_rn(x[j].w, p0[j].w);
+        }
+        if (two) {
+          x[j].x = __fadd_rn(x[j].x, p1[j].x), x[j].y = __fadd_rn(x[j].y, p1[j].y);
+          x[j].z = __fadd_rn(x[j].z, p1[j].z), x[j].w = __fadd_rn(x[j].w, p1[j].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ4; ++j) {
+      const int e = 128 * j + 4 * lane;
+      if (e < E) *reinterpret_cast<float4*>(a.logits_out + (size_t)t * E + e) = x[j];
+    }
+    __syncwarp();  // every lane's loads are consumed before their lines are invalidated
+    if (a.discard) {  // the warp's 512 bytes per (split, j): four 128-byte lines
+      for (int l = lane; l < a.S * NJ4 * 4; l += 32) {
+        const int s = l / (NJ4 * 4), r = l - s * NJ4 * 4, e0 = 128 * (r >> 2) + 32 * (r & 3);
+        if (e0 < E)
+          asm volatile("discard.global.L2 [%0], 128;" ::"l"(a.part + ((size_t)s * a.T + t) * E + e0) : "memory");
+      }
+    }
+  } else {
+    const float* lg = a.logits + (size_t)t * E;
+#pragma unroll
+    for (int j = 0; j < NJ4; ++j) {
+      const int e = 128 * j + 4 * lane;
+      x[j] = e < E ? __ldg(reinterpret_cast<const float4*>(lg + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+template <int NJ4, bool PART>
 __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, WarpScratch& ws) {
-  static_assert(NJ <= 32, "one flag bit per expert of a lane");
+  static_assert(4 * NJ4 <= 32, "one flag bit per expert of a lane");
+  constexpr int NJ = 4 * NJ4;
   const int lane = threadIdx.x & 31;
   const int E = a.E, K = a.K;
-  float x[NJ], b[NJ];
-  load_logits<NJ, PART>(a, t, lane, 32, x);
+  float4 x4[NJ4], b4[NJ4];
+  load_logits4<NJ4, PART>(a, t, x4);
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int e = lane + 32 * j;
-    b[j] = (a.bias && e < E) ? __ldg(a.bias + e) : 0.f;
+  for (int j = 0; j < NJ4; ++j) {
+    const int e = 128 * j + 4 * lane;
+    b4[j] = (a.bias && e < E) ? __ldg(reinterpret_cast<const float4*>(a.bias + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e < E) *reinterpret_cast<float4*>(&ws.x[e]) = x4[j];  // the row, for the candidates' exact keys
   }
-  // 1) approximate keys; the lane maximum
-  uint32_t key[NJ], m = 0;
+  // 1) approximate keys as floats (NaN never a candidate); the lane maximum
+  float c[NJ];
+  float m = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const float sv = approx_sigmoid(x[j]);
-    const float c = a.bias ? __fadd_rn(sv, b[j]) : sv;
-    key[j] = lane + 32 * j < E ? order_key(c) : 0u;
-    m = max(m, key[j]);
+  for (int j = 0; j < NJ4; ++j) {
+    const float xs[4] = {x4[j].x, x4[j].y, x4[j].z, x4[j].w}, bs[4] = {b4[j].x, b4[j].y, b4[j].z, b4[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float sv = approx_sigmoid(xs[i]);
+      c[4 * j + i] = 128 * j + 4 * lane < E ? (a.bias ? __fadd_rn(sv, bs[i]) : sv) : -INFINITY;
+      m = fmaxf(m, c[4 * j + i]);  // (ignores NaN)
+    }
   }
-  // 2) bound: the K-th largest of the 32 lane maxima (K different lanes hold a key at
-  //    least that large)
-  const uint32_t thr = candidate_threshold(__shfl_sync(kFull, warp_sort_desc(m), K - 1));
-  // 3) candidates: every expert at or above the threshold, counted and compacted in
-  //    lane order
+  // 2) bound: the K-th largest of the 32 lane maxima, sorted descending over shuffles
+  //    (-inf for a lane without a number)
+  float v = m != m ? -INFINITY : m;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(kFull, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  const float B = __shfl_sync(kFull, v, K - 1);
+  // every exact top-K expert has an approximate key within 2 err of the bound (err =
+  // kApproxErr plus an ulp or two of the key); a bound that is not a finite number
+  // sends the token to the all-exact path
+  const float thr = __fsub_rn(B, 2.0f * kApproxErr + 0x1p-21f * (1.0f + fabsf(B)));
+  // 3) candidates: counted, and compacted in lane order (their expert ids)
   uint32_t flags = 0;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (key[j] >= thr && key[j] != 0u) flags |= 1u << j;
+  for (int j = 0; j < NJ; ++j) flags |= (c[j] >= thr ? 1u : 0u) << j;
   const int mine = __popc(flags);
   int incl = mine;
 #pragma unroll
@@ -263,25 +337,26 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
     if (lane >= o) incl += y;
   }
   const int total = __shfl_sync(kFull, incl, 31);
-  if (total <= 64) {
+  if (isfinite(thr) && total >= K && total <= 64) {
     int pos = incl - mine;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      if (flags & (1u << j)) {
-        ws.e[pos] = lane + 32 * j;
-        ws.x[pos] = x[j];
-        ws.b[pos] = b[j];
-        ++pos;
-      }
+      if (flags & (1u << j)) ws.e[pos++] = 128 * (j >> 2) + 4 * lane + (j & 3);
     }
     __syncwarp();
-    // 4) exact keys of the candidates (lane i: candidates i and i + 32); the slot of a
-    //    candidate is the number of candidates ordering before it (keys made distinct
-    //    by the expert in the low word): independent comparisons over shuffles
+    // 4) exact keys of the candidates (lane i: candidates i and i + 32); a candidate's
+    //    slot is the number of candidates ordering before it (keys made distinct by the
+    //    expert in the low word): independent comparisons over shuffles
     unsigned long long c0 = 0, c1 = 0;
     float s0 = 0.f, s1 = 0.f;
-    if (lane < total) c0 = rank_key(exact_key(a, ws.x[lane], ws.b[lane], &s0), ws.e[lane]);
-    if (lane + 32 < total) c1 = rank_key(exact_key(a, ws.x[lane + 32], ws.b[lane + 32], &s1), ws.e[lane + 32]);
+    if (lane < total) {
+      const int e = ws.e[lane];
+      c0 = rank_key(exact_key(a, ws.x[e], a.bias ? __ldg(a.bias + e) : 0.f, &s0), e);
+    }
+    if (lane + 32 < total) {
+      const int e = ws.e[lane + 32];
+      c1 = rank_key(exact_key(a, ws.x[e], a.bias ? __ldg(a.bias + e) : 0.f, &s1), e);
+    }
     int r0 = 0, r1 = 0;
     if (total <= 32) {
 #pragma unroll
@@ -303,13 +378,18 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
       ws.slot_s[r1] = s1;
     }
   } else {
-    // heavy ties (more than 64 candidates): exact keys of all experts, then K rounds of
-    // a warp argmax over (key descending, expert ascending)
+    // heavy ties, NaN or infinite keys: exact keys of all experts, then K rounds of a
+    // warp argmax over (key descending, expert ascending)
+    uint32_t key[NJ];
     float sc[NJ];
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const uint32_t kx = exact_key(a, x[j], b[j], &sc[j]);
-      key[j] = lane + 32 * j < E ? kx : 0u;
+    for (int j = 0; j < NJ4; ++j) {
+      const float xs[4] = {x4[j].x, x4[j].y, x4[j].z, x4[j].w}, bs[4] = {b4[j].x, b4[j].y, b4[j].z, b4[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t kx = exact_key(a, xs[i], bs[i], &sc[4 * j + i]);
+        key[4 * j + i] = 128 * j + 4 * lane < E ? kx : 0u;
+      }
     }
     for (int k = 0; k < K; ++k) {
       uint32_t bk = 0;
@@ -319,20 +399,20 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
       for (int j = 0; j < NJ; ++j) {
         if (key[j] > bk) {  // ascending expert order within the lane: the first maximum wins
           bk = key[j];
-          be = lane + 32 * j;
+          be = 128 * (j >> 2) + 4 * lane + (j & 3);
           bs = sc[j];
         }
       }
       const uint32_t wk = __reduce_max_sync(kFull, bk);
       const int we = (int)__reduce_min_sync(kFull, bk == wk ? (uint32_t)be : 0x7FFFFFFFu);
-      const float wsv = __shfl_sync(kFull, bs, we & 31);  // expert e lives in lane e % 32
+      const float wsv = __shfl_sync(kFull, bs, (we >> 2) & 31);  // expert e lives in lane (e / 4) % 32
       if (lane == 0) {
         ws.slot_id[k] = we;
         ws.slot_s[k] = wsv;
       }
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
-        if (lane + 32 * j == we) key[j] = 0u;
+        if (128 * (j >> 2) + 4 * lane + (j & 3) == we) key[j] = 0u;
     }
   }
   __syncwarp();
@@ -341,8 +421,8 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
 }
 
 // ---------------------------------------------------------------------------------
-// One CTA of kThreads threads per token (kWarpMaxE < E <= 32 * kThreads). Thread i
-// holds the experts i + 128 j. The bound is the K-th largest of the 128 thread maxima
+// One CTA of kThreads threads per token (small batches, and any E <= 32 * kThreads).
+// Thread i holds the experts i + 128 j. The bound is the K-th largest of the 128 thread maxima
 // (each warp sorts its 32, two rounds of bitonic merges give the top 32 of all 128);
 // up to 32 candidates are ranked by warp 0 over shuffles, up to 64 by counting over
 // shared memory, more (heavy ties) by exact keys for all and K rounds of argmax.
@@ -529,9 +609,10 @@ __device__ __forceinline__ void topk_token_cta(const TopkArgs& a, const int t) {
   if (warp == 0) write_slots(a, t, slot_id, slot_s);
 }
 
-// The routing part of a launch: CTA `blk` of the routing CTAs. Warp body (E <=
-// kWarpMaxE): its 4 warps take tokens 4 blk .. 4 blk + 3; CTA body: token blk. Waits for
-// the preceding kernel (which writes the logits or partials) before reading.
+// The routing part of a launch: CTA `blk` of the routing CTAs. Warp body (NJ = experts
+// per lane / 4): its 4 warps take tokens 4 blk .. 4 blk + 3; CTA body (NJ = experts
+// per thread): token blk. Waits for the preceding kernel (which writes the logits or
+// partials) before reading.
 template <int NJ, bool WARP, bool PART>
 __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
   grid_launch_dependents();
@@ -547,6 +628,15 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
 
 // Routing CTAs for T tokens.
 __host__ __device__ constexpr int route_blocks(int T, bool warp) { return warp ? (T + kWarps - 1) / kWarps : T; }
+
+// Which body routes a launch. A token's four warps (CTA body) finish it sooner than one
+// warp does, so the CTA body takes small batches; from kWarpMinTokens tokens on the
+// warp body (a quarter of the instructions per token, no CTA barrier) does, when its
+// float4 layout applies: E <= kWarpMaxE, E % 4 == 0, 16-byte aligned rows and bias.
+constexpr int kWarpMinTokens = 192;
+inline bool use_warp_body(int T, int E, const void* rows, const float* bias) {
+  return T >= kWarpMinTokens && E <= kWarpMaxE && E % 4 == 0 && aligned(rows, 16) && (!bias || aligned(bias, 16));
+}
 
 }  // namespace topk_impl
 }  // namespace moe

@@ -67,6 +67,9 @@ def _load():
         lib.oracle_unit_windows.restype = I
         lib.oracle_mxfp8_quantize.argtypes = [P, I, I, P, P]
         lib.oracle_mxfp8_quantize_rule.argtypes = [P, I, I, I, P, P]
+        lib.oracle_mxfp8_tcgen05_scales_bytes.argtypes = [I, I]
+        lib.oracle_mxfp8_tcgen05_scales_bytes.restype = ctypes.c_size_t
+        lib.oracle_mxfp8_scales_tcgen05.argtypes = [P, I, I, P]
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -222,6 +225,17 @@ def mxfp8_quantize(x, rule=0):
     else:
         _load().oracle_mxfp8_quantize_rule(_ptr(x), rows, cols, int(rule), _ptr(q), _ptr(s))
     return q, s
+
+
+def mxfp8_scales_tcgen05(scales):
+    """Row-major E8M0 scales [rows, nsc] in the tcgen05 block-scaling tile layout
+    (128 x 4 tiles of 512 bytes, padding 0): a flat uint8 array."""
+    scales = _c(scales, np.uint8)
+    rows, nsc = scales.shape
+    lib = _load()
+    out = np.empty(lib.oracle_mxfp8_tcgen05_scales_bytes(rows, nsc), np.uint8)
+    lib.oracle_mxfp8_scales_tcgen05(_ptr(scales), rows, nsc, _ptr(out))
+    return out
 
 
 def e4m3_encode(y: float) -> int:

@@ -438,6 +438,33 @@ void oracle_mxfp8_quantize(const uint16_t* x, int rows, int cols, uint8_t* q,
   oracle_mxfp8_quantize_rule(x, rows, cols, 0, q, scales);
 }
 
+/* The scale bytes of oracle_mxfp8_quantize_rule in the tile layout that the
+ * block-scaled tensor-core MMA of the sm_100 family (tcgen05.mma kind::mxf8f6f4 with
+ * a scale vector of 32) loads through tcgen05.cp, as the PTX ISA and CUTLASS's
+ * block-scaled GEMMs describe it: the [rows, nsc] scale matrix is cut into tiles of
+ * 128 rows x 4 scale columns (rows padded to a multiple of 128, columns to a multiple
+ * of 4); tile (i, j) occupies the 512 bytes at (i * CT + j) * 512, CT = ceil(nsc / 4),
+ * and inside it the scale of row r (0..127) and column c (0..3) is byte
+ * 16 * (r mod 32) + 4 * (r div 32) + c: 32 lines of 16 bytes, line l holding rows
+ * l, l + 32, l + 64, l + 96. Padding bytes are 0. The wide page writes its plan rows
+ * with a swizzled scale layout of its own (plan_xsf) that it does not show. */
+size_t oracle_mxfp8_tcgen05_scales_bytes(int rows, int nsc) {
+  const size_t rt = (size_t)(rows + 127) / 128, ct = (size_t)(nsc + 3) / 4;
+  return rt * ct * 512;
+}
+
+void oracle_mxfp8_scales_tcgen05(const uint8_t* scales, int rows, int nsc, uint8_t* out) {
+  const size_t ct = (size_t)(nsc + 3) / 4;
+  memset(out, 0, oracle_mxfp8_tcgen05_scales_bytes(rows, nsc));
+  for (int r = 0; r < rows; ++r) {
+    for (int c = 0; c < nsc; ++c) {
+      const size_t tile = (size_t)(r / 128) * ct + (size_t)(c / 4);
+      const int rr = r % 128, cc = c % 4;
+      out[tile * 512 + 16 * (rr % 32) + 4 * (rr / 32) + cc] = scales[(size_t)r * nsc + c];
+    }
+  }
+}
+
 /* E4M3 byte -> value (NaN for 0x7F/0xFF). */
 double oracle_e4m3_decode(uint8_t c) {
   int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;

@@ -98,3 +98,21 @@ def test_bad_rule_rejected(moe):
     x = bf16_dev(synth.normal_bf16(1, 5, (2, 64)))
     with pytest.raises(moe.MoeError):
         moe.mxfp8_quantize_rows(x, scale_rule=2)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (1, 3584), (127, 96), (128, 128), (129, 3584), (1020, 3584),
+                                       (4096, 3584), (33, 288), (5, 7168)])
+@pytest.mark.parametrize("rule", [0, 1])
+def test_tcgen05_scale_layout(moe, orc, rows, cols, rule):
+    """Scales in the tcgen05 block-scaling tile layout, bit for bit against the oracle's
+    layout of its own scales (padding bytes 0); the E4M3 bytes equal the row-major
+    call's."""
+    x = synth.latent_rows(rows, seed=rows + cols)[:, :cols] if cols <= 3584 else synth.normal_bf16(5, 9, (rows, cols))
+    xd = bf16_dev(np.ascontiguousarray(x))
+    n = moe.mxfp8_tcgen05_scales_bytes(rows, cols)
+    sc = torch.full((n,), 0xA5, dtype=torch.uint8, device="cuda")  # padding must be written
+    q, sc = moe.mxfp8_quantize_rows_tcgen05(xd, scales=sc, scale_rule=rule)
+    torch.cuda.synchronize()
+    eq, es = orc.mxfp8_quantize(np.ascontiguousarray(x), rule)
+    np.testing.assert_array_equal(host(q), eq)
+    np.testing.assert_array_equal(host(sc), orc.mxfp8_scales_tcgen05(es))

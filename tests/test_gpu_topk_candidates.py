@@ -29,13 +29,15 @@ def test_approx_sigmoid_bound(tmp_path):
 
 @pytest.mark.parametrize("step_exp", [-11, -13, -15, -20])
 @pytest.mark.parametrize("with_bias", [False, True])
-def test_near_ties(moe, orc, step_exp, with_bias):
+@pytest.mark.parametrize("T", [64, 256])
+def test_near_ties(moe, orc, step_exp, with_bias, T):
     """Logits on a ladder 0.5 + i * 2^step_exp (shuffled over the experts): neighbouring
     scores differ by about 0.24 * 2^step_exp, near or below the approximation's error, so
     many experts fall inside the candidate margin (about 2^-10): 2^-11 gives ~25
     candidates (ranked over shuffles), 2^-13 ~50 (two per lane), 2^-15 and 2^-20 more
-    than 64 (exact keys for all, argmax rounds)."""
-    T, E, K = 64, 896, 16
+    than 64 (exact keys for all, argmax rounds). T = 64 takes the CTA-per-token body,
+    T = 256 the warp-per-token body."""
+    E, K = 896, 16
     rng = np.random.default_rng(100 - step_exp)
     lad = (0.5 + np.arange(E, dtype=np.float64) * 2.0 ** step_exp).astype(np.float32)
     logits = np.stack([lad[rng.permutation(E)] for _ in range(T)])

@@ -54,3 +54,23 @@ def test_whole_job_rate_counts_every_rank():
     assert bench.whole_job_rate(1020, 1, 1.0) == pytest.approx(1.02e6)
     assert bench.whole_job_rate(1020, 4, 1.0) == pytest.approx(4.08e6)
     assert bench.max_over_ranks([3.0, 4.0], 1, "cpu") == [3.0, 4.0]
+
+
+def test_reference_arm_reports_the_steps_it_ran():
+    """The reference arm's line states the warm-up and timed steps it actually ran: K
+    timed steps of ms_per_step each fit inside the call's own wall time, and the rate
+    is the step's tokens over that step time."""
+    import time
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    args = type("A", (), {"steps": 2, "warmup": 1, "cpu_seconds": 0.1})()
+    t0 = time.perf_counter()
+    line = bench.run_reference(args, 0)
+    wall = time.perf_counter() - t0
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["steps"] * line["ms_per_step"] / 1e3 <= wall
+    assert line["value"] == pytest.approx(bench.REF_TOKENS / (line["ms_per_step"] / 1e3), rel=1e-2)
+    assert set(line["cpu_baseline"]["per_step_ms"]) == set(bench.ORACLE_STEPS)
+    assert line["cpu_baseline"]["cores"] == 1 and line["cpu_baseline"]["nproc"] >= 1

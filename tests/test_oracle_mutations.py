@@ -45,6 +45,9 @@ MUTATIONS = {
     "norm_eps_outside": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);", "const double inv = 1.0 / (sqrt(ss / (double)H) + eps);"),
     "norm_no_gamma": ("* inv * (double)bf16_to_f32(g[c]);", "* inv;"),
     "mx_ceil_always_up": ("if (rule == 1 && (double)amax > ldexp(448.0, se)) se += 1;", "if (rule == 1) se += 1;"),
+    "mx_tiles_line_swap": ("out[tile * 512 + 16 * (rr % 32) + 4 * (rr / 32) + cc]", "out[tile * 512 + 4 * (rr % 32) + 16 * (rr / 32) + cc]"),
+    "mx_tiles_column_major": ("const size_t tile = (size_t)(r / 128) * ct + (size_t)(c / 4);",
+                              "const size_t tile = (size_t)(c / 4) * ((size_t)(rows + 127) / 128) + (size_t)(r / 128);"),
     "mx_ceil_at_448": ("if (rule == 1 && (double)amax > ldexp(448.0, se)) se += 1;",
                        "if (rule == 1 && (double)amax >= ldexp(448.0, se)) se += 1;"),
 }

@@ -157,3 +157,42 @@ def test_ceil_rule_matches_floor_below_1_75(orc):
     assert keep.sum() >= 16
     np.testing.assert_array_equal(s1[keep], s0[keep])
     np.testing.assert_array_equal(q1[keep], q0[keep])
+
+
+# ---------------------------------------------------------------------------
+# The tcgen05 block-scaling tile layout of the scales (128 rows x 4 scale columns per
+# 512-byte tile; inside a tile, row r and column c at 16 * (r % 32) + 4 * (r // 32) + c;
+# tiles ordered row tile by row tile; padding 0).
+
+def test_tcgen05_scale_layout_closed_forms(orc):
+    """Positions worked out by hand for a 130 x 5 scale matrix (two row tiles, two
+    column tiles: 2048 bytes), each scale byte distinct so that its position shows."""
+    rows, nsc = 130, 5
+    sc = (np.arange(rows * nsc) % 251 + 1).astype(np.uint8).reshape(rows, nsc)  # never 0
+    t = orc.mxfp8_scales_tcgen05(sc)
+    assert t.size == 2048
+    expect = {  # (row, scale column) -> byte offset
+        (0, 0): 0, (1, 0): 16, (31, 0): 496, (32, 0): 4, (33, 1): 21, (64, 2): 10, (96, 3): 15,
+        (127, 3): 511, (0, 4): 512, (5, 4): 592, (100, 4): 512 + 16 * 4 + 4 * 3, (128, 0): 1024,
+        (129, 3): 1024 + 16 + 3, (128, 4): 1536, (129, 4): 1552,
+    }
+    for (r, c), off in expect.items():
+        assert t[off] == sc[r, c], (r, c, off)
+
+
+def test_tcgen05_scale_layout_covers_every_scale_once(orc):
+    """Every scale lands in its own byte; the remaining bytes (padding rows and columns)
+    are 0; the layout reads back to the row-major matrix."""
+    for rows, nsc in ((1, 1), (127, 4), (128, 4), (129, 7), (300, 112), (1020, 112)):
+        sc = np.random.default_rng(rows * 1000 + nsc).integers(1, 256, (rows, nsc)).astype(np.uint8)
+        t = orc.mxfp8_scales_tcgen05(sc)
+        rt, ct = -(-rows // 128), -(-nsc // 4)
+        assert t.size == rt * ct * 512
+        r, c = np.meshgrid(np.arange(rows), np.arange(nsc), indexing="ij")
+        off = ((r // 128) * ct + c // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + c % 4
+        assert np.unique(off).size == rows * nsc
+        np.testing.assert_array_equal(t[off], sc)
+        pad = np.ones(t.size, bool)
+        pad[off.ravel()] = False
+        assert not t[pad].any()
+        assert pad.sum() == t.size - rows * nsc
