@@ -10,6 +10,10 @@ void simt_plan(int T, int H, int E, int sm_count, int* S, int* kc);
 int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int S, int kc,
                        float* part, cudaStream_t stream);
 
+// CUDA-core GEMV for T <= kGemvMaxTokens: no split-K, no workspace, one launch.
+constexpr int kGemvMaxTokens = 8;
+int launch_router_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, cudaStream_t stream);
+
 // Tensor-core (tcgen05) split-K path.
 struct TcPlan {
   int bn;    // token tile: 16, 32, 64, 128 or 256

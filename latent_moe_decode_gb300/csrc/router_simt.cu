@@ -13,6 +13,7 @@
 // 32 lane partials of the warp's 32 outputs are combined by a transposing butterfly
 // (31 shuffles), after which lane l holds output l. Split-K partials go to the
 // workspace and a second kernel sums them in split order (deterministic).
+// For at most 8 tokens the GEMV form below takes over: no split-K and no second kernel.
 #include "router.cuh"
 
 namespace moe {
@@ -76,6 +77,88 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
   if (e < E && t < T) out[((size_t)s * T + t) * E + e] = acc[0];
 }
 
+// GEMV form for T <= 8 tokens (TT: the tokens rounded up to 1, 2, 4 or 8): the 12.8 MB
+// gate is one HBM stream and the tokens' rows are small, so no K is split and no
+// partials leave the CTA. A CTA of kGemvWarps warps owns kGemvRows expert rows over the
+// whole hidden dimension; the 16-byte fragments f of a row are dealt to warps in runs
+// of 32 (warp (f / 32) % kGemvWarps, lane f % 32), so every load instruction of a warp
+// reads 512 contiguous bytes of a gate row. A lane accumulates its products (at most
+// H / 224 fragments x 8 = 32 at H = 7168) per output in FP32 in hidden order, each
+// warp's 32 lane sums are combined by a fixed shuffle tree, and the warps' sums in warp
+// order: deterministic. The CTA first asks L2 to prefetch its gate rows (weights may be
+// read before the wait for the preceding kernel only as a prefetch) so the stream
+// starts while the preceding kernel finishes.
+constexpr int kGemvWarps = 7;
+constexpr int kGemvRows = 2;
+
+template <int TT>
+__global__ void __launch_bounds__(kGemvWarps * 32) router_gemv_kernel(const uint16_t* __restrict__ x,
+                                                                      const uint16_t* __restrict__ w,
+                                                                      float* __restrict__ out, int T, int H, int E) {
+  __shared__ float red[kGemvWarps][kGemvRows * TT];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e0 = blockIdx.x * kGemvRows;
+  const int F = H / 8;                                           // 16-byte fragments per row
+  const int NI = (F + 32 * kGemvWarps - 1) / (32 * kGemvWarps);  // fragments per lane
+  const uint16_t* wr[kGemvRows];
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r) wr[r] = w + (size_t)min(e0 + r, E - 1) * H;
+  for (int i = 0; i < NI; ++i) {
+    const int f = lane + 32 * (warp + kGemvWarps * i);
+    if (f < F)
+#pragma unroll
+      for (int r = 0; r < kGemvRows; ++r) asm volatile("prefetch.global.L2 [%0];" ::"l"(wr[r] + f * 8));
+  }
+  grid_launch_dependents();
+  grid_wait();
+  float acc[kGemvRows][TT];
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
+#pragma unroll(TT <= 2 ? 4 : 2)
+  for (int i = 0; i < NI; ++i) {
+    const int f = lane + 32 * (warp + kGemvWarps * i);
+    if (f >= F) break;
+    uint4 wv[kGemvRows], xv[TT];
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r) wv[r] = ld_nc16(wr[r] + f * 8);
+#pragma unroll
+    for (int t = 0; t < TT; ++t) xv[t] = t < T ? ld_nc16(x + (size_t)t * H + f * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r) {
+      const uint32_t a4[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const uint32_t b4[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[r][t] = __fmaf_rn(bf16_lo(a4[j]), bf16_lo(b4[j]), acc[r][t]);
+          acc[r][t] = __fmaf_rn(bf16_hi(a4[j]), bf16_hi(b4[j]), acc[r][t]);
+        }
+      }
+    }
+  }
+  // the warp's sum of each output: a fixed xor tree over the lanes
+#pragma unroll
+  for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      float v = acc[r][t];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
+      if (lane == 0) red[warp][r * TT + t] = v;
+    }
+  __syncthreads();
+  if (threadIdx.x < kGemvRows * TT) {
+    const int r = threadIdx.x / TT, t = threadIdx.x - r * TT, e = e0 + r;
+    float v = red[0][threadIdx.x];
+#pragma unroll
+    for (int q = 1; q < kGemvWarps; ++q) v = __fadd_rn(v, red[q][threadIdx.x]);
+    if (t < T && e < E) out[(size_t)t * E + e] = v;
+  }
+}
+
 __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ part, int S, long long n,
                                                             float* __restrict__ logits) {
   grid_wait();
@@ -111,6 +194,15 @@ int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int 
   int st = launch_pdl(router_simt_kernel, grid, dim3(kThreads), smem, stream, x, w, S == 1 ? logits : part, T, H, E, kc);
   if (st != MOE_OK || S == 1) return st;
   return launch_router_reduce(part, S, T, E, logits, stream);
+}
+
+int launch_router_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, cudaStream_t stream) {
+  const dim3 grid((E + kGemvRows - 1) / kGemvRows), block(kGemvWarps * 32);
+  if (T <= 1) return launch_pdl(router_gemv_kernel<1>, grid, block, 0, stream, x, w, logits, T, H, E);
+  if (T <= 2) return launch_pdl(router_gemv_kernel<2>, grid, block, 0, stream, x, w, logits, T, H, E);
+  if (T <= 4) return launch_pdl(router_gemv_kernel<4>, grid, block, 0, stream, x, w, logits, T, H, E);
+  if (T <= kGemvMaxTokens) return launch_pdl(router_gemv_kernel<8>, grid, block, 0, stream, x, w, logits, T, H, E);
+  return MOE_ERR_INVALID_ARGUMENT;
 }
 
 int launch_router_reduce(const float* part, int S, int T, int E, float* logits, cudaStream_t stream) {

@@ -218,7 +218,7 @@ __device__ __forceinline__ void write_slots(const TopkArgs& a, int t, const int3
 // One warp per token (E <= kWarpMaxE, E % 4 == 0, 16-byte aligned rows). Lane l holds
 // the experts 128 j + 4 l + i (j < NJ4, i < 4): one 16-byte load per j, so a load
 // instruction of the warp reads 512 contiguous bytes of the logits row.
-struct WarpScratch {
+struct __align__(16) WarpScratch {  // (16: the logits row is stored as float4)
   float x[kWarpMaxE];  // the token's logits (exact keys of the candidates read them here)
   int32_t e[64];       // candidates (at most 64 take the ranking paths)
   int32_t slot_id[MOE_MAX_TOPK];
