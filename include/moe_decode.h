@@ -92,18 +92,23 @@ int moe_device_error(uint32_t* bits, int clear);
  *             matter and are clobbered. Calls that share a workspace must not overlap.
  * Requirements: T >= 1, E >= 1, H >= 8, H % 8 == 0; x, w 16-byte aligned
  * (MOE_ERR_ALIGNMENT), logits 4-byte aligned.
- * Numerics: BF16 products are exact in FP32; sums are accumulated in FP32 on the tensor
- * cores in K-chunks, the split-K partials reduced in a fixed order, so the result is
- * deterministic run to run. The error is well inside 1e-5 * sum_j |x[t,j] w[e,j]|.
+ * Numerics: BF16 products are exact in FP32; sums are accumulated in FP32 -- for up
+ * to 8 tokens on the CUDA cores (one pass over the gate, no split-K: per-lane chains
+ * of at most H / 224 fragments x 8 products, then fixed shuffle and warp trees), else
+ * on the tensor cores in K-chunks with the split-K partials reduced in a fixed order
+ * -- so the result is deterministic run to run. The error is well inside
+ * 1e-5 * sum_j |x[t,j] w[e,j]|.
  * ------------------------------------------------------------------------------- */
 size_t moe_router_logits_workspace(int T, int H, int E);
 int moe_router_logits(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E,
                       void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* The same computation with an explicit kernel family: MOE_ROUTER_AUTO (what
- * moe_router_logits uses), MOE_ROUTER_SIMT (CUDA-core split-K, per-lane FP32 chains of
- * at most 128 products, then a fixed butterfly) or MOE_ROUTER_TCGEN05 (tensor-core
- * split-K with a TMEM accumulator). The workspace query covers every family. */
+ * moe_router_logits uses: the CUDA cores for T <= 8, the tensor cores above),
+ * MOE_ROUTER_SIMT (CUDA cores: the GEMV form for T <= 8, else split-K with per-lane
+ * FP32 chains of at most 128 products and a fixed butterfly) or MOE_ROUTER_TCGEN05
+ * (tensor-core split-K with a TMEM accumulator). The workspace query covers every
+ * family. */
 #define MOE_ROUTER_AUTO 0
 #define MOE_ROUTER_SIMT 1
 #define MOE_ROUTER_TCGEN05 2
@@ -375,7 +380,7 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  * Source: [wide] WideMoE.run (router logits -> route -> ... -> Finalize of the
  * token's top-K expert rows, on one stream) and [ep] EpMoeLayer.__call__.
  *
- * Launches, on `stream`, in this order (programmatic dependent launch between them):
+ * Computes, on `stream`, what these four calls compute, in this order:
  *   moe_router_logits(x, w, logits, T, H, E, workspace, ...)
  *   moe_topk_route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights,
  *                           weights_bf16, latent, T, L, q, scales)
@@ -383,14 +388,18 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  *   moe_finalize(rows, T*K, NULL, weights_bf16, MOE_DTYPE_BF16, NULL, 1, T, K, L, out)
  * i.e. Finalize combines the expanded expert rows (row t*K + k = token t's k-th
  * expert) with the BF16 routing weights, as the wide page's Finalize does. Every
- * output equals the four calls' bit for bit. (For token tiles wider than 64 the router
- * stores its split-K partials in the workspace instead of reducing them, and the top-K
- * launch sums each token's partials in the same split order before selecting: the
- * same logits, one on-chip exchange fewer.) Arguments, layouts and requirements are
- * those of the four calls (weights may be NULL; weights_bf16 may not). `workspace` holds moe_route_finalize_workspace(T, H, E, K)
- * bytes (NULL when that is 0); it is clobbered. Returns the first non-OK status of the
- * four calls (the later ones are then not launched). Allocates nothing, so the call
- * can be captured in a CUDA graph.
+ * output equals the four calls' bit for bit. It takes three launches (programmatic
+ * dependent launch between them): the router; top-K with the MXFP8 of the latent; and
+ * Finalize, whose launch also builds the routing lists in CTAs of its own (Finalize
+ * does not read them, so they are built beside its row stream). For token tiles wider
+ * than 64 the router stores its split-K partials in the workspace instead of reducing
+ * them, and the top-K launch sums each token's partials in the same split order before
+ * selecting: the same logits, one on-chip exchange fewer. Arguments, layouts and
+ * requirements are those of the four calls (weights may be NULL; weights_bf16 may
+ * not); they are all checked before the first launch. `workspace` holds
+ * moe_route_finalize_workspace(T, H, E, K) bytes (NULL when that is 0); it is
+ * clobbered. Returns the first non-OK status (nothing is launched after it). Allocates
+ * nothing, so the call can be captured in a CUDA graph.
  * ------------------------------------------------------------------------------- */
 size_t moe_route_finalize_workspace(int T, int H, int E, int K);
 int moe_route_finalize(const uint16_t* x, const uint16_t* w, const float* bias, const uint16_t* latent,

@@ -376,8 +376,8 @@ def route_finalize(x, w, bias, latent, rows, K: int, renormalize: bool, scale: f
 class RouteFinalize:
     """The whole routing-and-combine step, with its buffers preallocated:
     router logits -> sigmoid+bias top-K with the MXFP8 latent in the same launch ->
-    routing lists -> Finalize, on one stream (Finalize does not read the lists and
-    starts streaming its rows while they are built).
+    Finalize, whose launch also builds the routing lists (Finalize does not read them),
+    on one stream.
 
     ``run()`` launches the library's kernels (programmatic dependent launch between
     consecutive kernels of a stream) and allocates nothing, so it can be captured in a
@@ -409,8 +409,8 @@ class RouteFinalize:
         """Kernels one run() launches."""
         if self.router_algo == ROUTER_AUTO:
             # the one-call step: router (its split-K partials summed by the top-K launch),
-            # top-k + MXFP8, lists, Finalize
-            return 4
+            # top-k + MXFP8, Finalize with the routing lists
+            return 3
         # the four calls; a forced router family may add its split-K reduce kernel
         return 4 + (1 if router_logits_workspace(self.T, self.H, self.E) > 0 else 0)
 

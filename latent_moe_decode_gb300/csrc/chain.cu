@@ -1,11 +1,11 @@
-// The routing-and-combine step as one call: the four launches of the chain, in order,
-// on the caller's stream. The router is launched the ordinary way (it starts once its
-// predecessor has completed) and signals its dependents after that; the later kernels
-// use programmatic dependent launch and execute griddepcontrol.wait before they read
-// anything an earlier kernel of the step wrote. Reads of the step's own inputs may come
-// first: the MXFP8 CTAs quantise the latent without waiting, and Finalize issues its
-// first row copies before its wait (and reads top-K's weights only after it), so the
-// rows stream in while the lists kernel runs.
+// The routing-and-combine step as one call: three launches on the caller's stream --
+// the router; top-K with the MXFP8 of the latent; Finalize with the routing lists. The
+// router is launched the ordinary way (it starts once its predecessor has completed)
+// and signals its dependents after that; the later kernels use programmatic dependent
+// launch and execute griddepcontrol.wait before they read anything an earlier kernel
+// of the step wrote. Reads of the step's own inputs may come first: the MXFP8 CTAs
+// quantise the latent without waiting, and Finalize issues its first row copies before
+// its wait (and reads top-K's weights only after it).
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideMoE.run
 // (router -> route -> Finalize on one stream) and ...moe.ep.layer, EpMoeLayer.__call__.
@@ -34,8 +34,11 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   using namespace moe;
   if (T < 1 || K < 1 || !weights_bf16) return MOE_ERR_INVALID_ARGUMENT;
   if (E < 1 || H < 8 || H % 8 != 0 || (long long)T * E > (1LL << 40)) return MOE_ERR_INVALID_ARGUMENT;
-  if (!x || !w || !logits) return MOE_ERR_INVALID_ARGUMENT;
+  if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK || K > E) return K > E ? MOE_ERR_INVALID_ARGUMENT : MOE_ERR_CAPACITY;
+  if (!x || !w || !logits || !ids || !offsets || !pairs || !rows || !out) return MOE_ERR_INVALID_ARGUMENT;
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(logits, 4)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(offsets, 4) || !aligned(pairs, 4))
+    return MOE_ERR_ALIGNMENT;
   const size_t rws = router_part_bytes(T, H, E);
   const size_t lws = moe_build_routing_lists_workspace(T, K, E);
   if (workspace_bytes < rws + lws || (rws + lws > 0 && !workspace)) return MOE_ERR_WORKSPACE;
@@ -56,10 +59,9 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
                       true, as_cuda(stream), S > 1 ? part : nullptr, S);
   if (st != MOE_OK) return st;
-  st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws : nullptr, lws, stream);
-  if (st != MOE_OK) return st;
-  // Finalize starts its row copies (a step input) before its wait, and reads top-K's
-  // weights after it, once the lists kernel (which itself waited for top-K) is complete.
-  return moe::finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out, true,
-                       moe::as_cuda(stream));
+  // Finalize starts its row copies (a step input) before its wait and reads top-K's
+  // weights after it; the same launch builds the routing lists of top-K's ids in CTAs
+  // of its own (one per 32 experts), beside the row stream, so the lists cost the step
+  // no launch and no time on its critical path.
+  return moe::finalize_with_lists(rows, weights_bf16, T, K, L, out, ids, E, offsets, pairs, moe::as_cuda(stream));
 }

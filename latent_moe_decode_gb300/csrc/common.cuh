@@ -45,9 +45,17 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
              const uint16_t* shared, float routed_scaling_factor, int T, int K, int H, uint16_t* out,
              bool rows_ready, cudaStream_t s);
 
+// Finalize of the one-call step (rows t*K + k with BF16 weights, the rows complete
+// before the preceding kernel started) whose launch also builds the routing lists of
+// ids (offsets, pairs) in CTAs of its own, beside the row stream.
+int finalize_with_lists(const uint16_t* rows, const uint16_t* weights_bf16, int T, int K, int H, uint16_t* out,
+                        const int32_t* ids, int E, int32_t* offsets, int32_t* pairs, cudaStream_t s);
+
 inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
-inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+__host__ __device__ inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
 
 // Launch `kernel` on `stream` with programmatic stream serialization allowed, so it
 // may start while its predecessor is still running; every kernel of this library
@@ -177,6 +185,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16) from global address src (16-byte
+// aligned). A hint with no effect on results: safe before griddepcontrol.wait even for
+// data the preceding kernel writes (L2 is where writes and reads meet; nothing lands in
+// registers or shared memory).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global

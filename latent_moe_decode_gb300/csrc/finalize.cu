@@ -26,8 +26,9 @@
 // one-call step: the preceding kernels make only the weights), the first two items'
 // row copies are issued before griddepcontrol.wait and their weights are read after
 // it, so the first 30 MB of rows stream in while the preceding kernel finishes.
-#include "common.cuh"
 #include <type_traits>
+
+#include "lists.cuh"
 
 namespace moe {
 namespace {
@@ -48,6 +49,10 @@ struct FinArgs {
   // shared rows) were complete before the preceding kernel started, so the first row
   // copies are issued before the wait, and the weights (and indices) after it
   int wait_all;
+  // LISTS instantiations: the first n_list CTAs build the routing lists of la (one
+  // 32-expert range each) instead of summing rows
+  lists_impl::ListArgs la;
+  int n_list;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
@@ -62,20 +67,46 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr int kStages = 2;
 
-// KT: compile-time K (0 = runtime K, up to MOE_MAX_TOPK).
-template <int KT, bool GATHER, bool BF16W, bool SHARED>
+// KT: compile-time K (0 = runtime K, up to MOE_MAX_TOPK). LISTS: the launch also builds
+// the routing lists (the one-call step): its first a.n_list CTAs do that, beside the
+// row stream, and the others run Finalize.
+template <int KT, bool GATHER, bool BF16W, bool SHARED, bool LISTS = false>
 __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   extern __shared__ __align__(16) uint4 slots[];  // [kStages][K (+1 shared)][kThreads]
+  int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
+  if constexpr (LISTS) {
+    if (cta < a.n_list) {
+      grid_launch_dependents();
+      grid_wait();  // the ids come from the preceding kernel
+      lists_impl::lists_range_cta<kThreads / 32>(a.la, cta,
+                                                 *reinterpret_cast<lists_impl::RangeSmem<kThreads / 32>*>(slots));
+      return;
+    }
+    cta -= a.n_list;
+    ncta -= a.n_list;
+  }
   constexpr int KM = KT ? KT : MOE_MAX_TOPK;
   const int K = KT ? KT : a.K;
   const int frags = a.H >> 3;
   const long long total = (long long)a.T * frags;
-  const long long stride = (long long)gridDim.x * kThreads;
-  const long long f0 = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const long long stride = (long long)ncta * kThreads;
+  const long long f0 = (long long)cta * kThreads + threadIdx.x;
   const size_t H = (size_t)a.H;
   grid_launch_dependents();
   // indices choose the rows to copy: with a gather, everything waits
   const bool early = !a.wait_all && !GATHER;
+  if (!GATHER && !early && threadIdx.x < K) {
+    // the CTA's first fragments (128 consecutive ones, at most two tokens) of row k:
+    // their DRAM fetch overlaps the preceding kernel's end (a hint only)
+    const long long lo = (long long)cta * kThreads, hi = min(lo + kThreads, total);
+    for (long long f = lo; f < hi;) {
+      const int t = (int)(f / frags);
+      const long long end = min(hi, (long long)(t + 1) * frags);
+      prefetch_l2(a.rows + ((size_t)t * K + threadIdx.x) * a.H + (size_t)(f - (long long)t * frags) * 8,
+                  (uint32_t)(end - f) * 16u);
+      f = end;
+    }
+  }
   if (!early) grid_wait();
   const uint64_t pol = policy_evict_first();
   const uint32_t base = smem_u32(slots) + threadIdx.x * 16u;
@@ -198,17 +229,21 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   cp_async_wait<0>();
 }
 
-template <int KT, bool G, bool B, bool S>
+template <int KT, bool G, bool B, bool S, bool LISTS = false>
 int launch_one(const FinArgs& a, int sm_count, cudaStream_t s) {
-  const size_t smem = (size_t)kStages * ((KT ? KT : a.K) + (S ? 1 : 0)) * kThreads * 16;
-  auto kern = finalize_kernel<KT, G, B, S>;
+  size_t smem = (size_t)kStages * ((KT ? KT : a.K) + (S ? 1 : 0)) * kThreads * 16;
+  if (LISTS && smem < sizeof(lists_impl::RangeSmem<kThreads / 32>)) smem = sizeof(lists_impl::RangeSmem<kThreads / 32>);
+  auto kern = finalize_kernel<KT, G, B, S, LISTS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
     return MOE_ERR_CUDA;
   const long long threads = (long long)a.T * (a.H / 8);
   const long long need = (threads + kThreads - 1) / kThreads;
-  const long long grid = need < (long long)sm_count * per_sm ? need : (long long)sm_count * per_sm;
+  // persistent: every CTA resident at once (the list CTAs included)
+  long long room = (long long)sm_count * per_sm - (LISTS ? a.n_list : 0);
+  if (room < 1) room = 1;
+  const long long grid = (need < room ? need : room) + (LISTS ? a.n_list : 0);
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, a);
 }
 
@@ -256,6 +291,29 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
   if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, dev.sm_count, s);
   if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, dev.sm_count, s);
   return launch_variant<0>(a, gather, bf16w, sh, dev.sm_count, s);
+}
+
+// Finalize of the one-call step (rows t*K + k, BF16 weights; rows ready before the
+// preceding kernel started) with the routing lists of `ids` built by the same launch.
+int finalize_with_lists(const uint16_t* rows, const uint16_t* weights_bf16, int T, int K, int H, uint16_t* out,
+                        const int32_t* ids, int E, int32_t* offsets, int32_t* pairs, cudaStream_t s) {
+  if (T < 1 || K < 1 || K > MOE_MAX_TOPK || H < 8 || H % 8 != 0 || E < 1 || E > MOE_MAX_EXPERTS)
+    return MOE_ERR_INVALID_ARGUMENT;
+  if ((long long)T * K > (1LL << 31) - 1 || (long long)T * (H / 8) > (1LL << 31) * (long long)kThreads - 1)
+    return MOE_ERR_CAPACITY;
+  if (!rows || !weights_bf16 || !out || !ids || !offsets || !pairs) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(weights_bf16, 2) || !aligned(ids, 4) ||
+      !aligned(offsets, 4) || !aligned(pairs, 4))
+    return MOE_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != MOE_OK) return st;
+  FinArgs a{rows, (long long)T * K, nullptr, weights_bf16, nullptr, 1.0f, T, K, H, out, dev.error_word, 0};
+  a.la = lists_impl::ListArgs{ids, T * K, E, lists_impl::kMaxEpc, offsets, pairs, dev.error_word};
+  a.n_list = (E + lists_impl::kMaxEpc - 1) / lists_impl::kMaxEpc;
+  if (K == 16) return launch_one<16, false, true, false, true>(a, dev.sm_count, s);
+  if (K == 8) return launch_one<8, false, true, false, true>(a, dev.sm_count, s);
+  return launch_one<0, false, true, false, true>(a, dev.sm_count, s);
 }
 
 }  // namespace moe

@@ -29,122 +29,15 @@
 // the steps' group sizes into per-step starts, and every match is then written in
 // parallel -- lists in ascending index order. No workspace and no atomics (shared or
 // global): the counts and placements come from warp votes and single-writer tables.
-#include "common.cuh"
+#include "lists.cuh"
 
 namespace moe {
 namespace {
 
+using namespace lists_impl;
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCluster = 8;  // CTAs sharing one expert range, one chunk of the ids each
-constexpr int kMaxEpc = 32;  // experts per CTA
-constexpr int kBatch = 16;   // steps (32 ids each) in flight per warp
-constexpr int kHeld = 16;    // steps whose owned slots stay in registers
-constexpr unsigned kFull = 0xFFFFFFFFu;
-
-struct ListArgs {
-  const int32_t* ids;
-  int n;  // T * K
-  int E, epc;
-  int32_t* offsets;
-  int32_t* pairs;
-  uint32_t* err;
-};
-
-struct Scan {
-  int e_lo, nexp, n;
-  int below = 0;
-  bool bad = false;
-  uint32_t held[kHeld / 4];  // byte s%4 of held[s/4]: owned slot of step s's id, 0xFF = none
-};
-
-// Pass 1 over kBatch steps from flat id b0 (+ lane); CHECK also flags ids outside [0, E).
-// Within each step the lanes holding an owned expert are grouped by it
-// (__match_any_sync) and the group's lowest lane writes the group size to
-// tab[step][expert] -- one writer per cell, no atomics; lane j then adds column j (its
-// expert) to its count.
-template <bool CHECK, bool HOLD>
-__device__ __forceinline__ void count_batch(const ListArgs& a, Scan& sc, int b0, int r1, int lane,
-                                            uint16_t (*tab)[kMaxEpc], int& count, int step0) {
-  int v[kBatch];
-#pragma unroll
-  for (int u = 0; u < kBatch; ++u) {
-    const int i = b0 + 32 * u + lane;
-    v[u] = i < r1 ? __ldg(a.ids + i) : -1;  // -1: never below e_lo, never owned
-    if (CHECK && i < r1 && (unsigned)v[u] >= (unsigned)a.E) sc.bad = true;
-  }
-#pragma unroll
-  for (int u = 0; u < kBatch; ++u) tab[u][lane] = 0;
-  __syncwarp();
-#pragma unroll
-  for (int u = 0; u < kBatch; ++u) {
-    sc.below += (unsigned)v[u] < (unsigned)sc.e_lo;
-    const unsigned jv = (unsigned)(v[u] - sc.e_lo);
-    const bool m = jv < (unsigned)sc.nexp;
-    const unsigned bal = __ballot_sync(kFull, m);
-    if (m) {
-      const unsigned peers = __match_any_sync(bal, jv);
-      if ((peers & ((1u << lane) - 1u)) == 0) tab[u][jv] = (uint16_t)__popc(peers);
-      if (HOLD) {
-        const int st = step0 + u;
-        sc.held[st / 4] &= ~((~jv & 0xFFu) << (8 * (st % 4)));
-      }
-    }
-  }
-  __syncwarp();
-#pragma unroll
-  for (int u = 0; u < kBatch; ++u) count += tab[u][lane];
-  __syncwarp();
-}
-
-// Pass 2 for one block of up to kBatch steps of a warp: the ids i0 + 32*st + lane, with
-// owned slots in the bytes of slot[] (0xFF = none). (1) Within each step, the matching
-// lanes are grouped by expert (__match_any_sync); a lane's rank is the count of its
-// group's lanes below it, and the group's lowest lane records the group size in
-// tab[st][expert]. The steps do not depend on one another. (2) Lane j turns column j
-// of tab into exclusive prefixes over the steps. (3) Every match is written at
-// base[expert] + run[expert] + tab[st][expert] + rank; lane j then advances run[j].
-__device__ __forceinline__ void place_block(const ListArgs& a, const uint32_t (&slot)[kBatch / 4], int i0, int nsteps,
-                                            int nexp, int lane, uint16_t (*tab)[kMaxEpc], int* run, const int* base) {
-#pragma unroll
-  for (int st = 0; st < kBatch; ++st) tab[st][lane] = 0;
-  __syncwarp();
-  uint32_t rk[kBatch / 4] = {};
-#pragma unroll
-  for (int st = 0; st < kBatch; ++st) {
-    if (st >= nsteps) break;  // warp-uniform
-    const unsigned jv = (slot[st / 4] >> (8 * (st % 4))) & 0xFFu;
-    const bool m = jv < (unsigned)nexp;
-    const unsigned bal = __ballot_sync(kFull, m);
-    if (m) {
-      const unsigned peers = __match_any_sync(bal, jv);
-      const unsigned r = __popc(peers & ((1u << lane) - 1u));
-      rk[st / 4] |= r << (8 * (st % 4));
-      if (r == 0) tab[st][jv] = (uint16_t)__popc(peers);
-    }
-  }
-  __syncwarp();
-  int total = 0;
-#pragma unroll
-  for (int st = 0; st < kBatch; ++st) {
-    const int c = tab[st][lane];
-    tab[st][lane] = (uint16_t)total;
-    total += c;
-  }
-  __syncwarp();
-#pragma unroll
-  for (int st = 0; st < kBatch; ++st) {
-    if (st >= nsteps) break;  // warp-uniform
-    const unsigned jv = (slot[st / 4] >> (8 * (st % 4))) & 0xFFu;
-    if (jv < (unsigned)nexp) {
-      const int r = (int)((rk[st / 4] >> (8 * (st % 4))) & 0xFFu);
-      a.pairs[base[jv] + run[jv] + tab[st][jv] + r] = i0 + 32 * st + lane;
-    }
-  }
-  __syncwarp();
-  run[lane] += total;
-  __syncwarp();
-}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -188,22 +81,17 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
   static_assert(kMaxEpc == 32 && kWarps == 16, "one lane per owned expert; two expert columns per warp");
   static_assert(kHeld == kBatch && kBatch % 4 == 0, "held steps are one pass-2 block");
 
+  // this CTA's ids: their DRAM fetch overlaps the preceding kernel's end (a hint only)
+  if (threadIdx.x == 0 && c1 - c0 >= 4 && ((reinterpret_cast<uintptr_t>(a.ids + c0) & 15) == 0))
+    prefetch_l2(a.ids + c0, (uint32_t)((c1 - c0) & ~3) * 4u);
   grid_wait();
   grid_launch_dependents();  // after the wait: dependents may rely on all before the lists
 
   // pass 1: lane j counts this warp's matches of owned expert j
   int* cnt = s_cnt[warp];
   uint16_t(*tab)[kMaxEpc] = s_tab[warp];
-  int count = 0;
   const bool check = blockIdx.y == 0;  // the first expert range's cluster checks every id once
-  if (r0 < r1) {
-    if (check) count_batch<true, true>(a, sc, r0, r1, lane, tab, count, 0);
-    else count_batch<false, true>(a, sc, r0, r1, lane, tab, count, 0);
-  }
-  for (int b0 = r0 + 32 * kHeld; b0 < r1; b0 += 32 * kBatch) {
-    if (check) count_batch<true, false>(a, sc, b0, r1, lane, tab, count, 0);
-    else count_batch<false, false>(a, sc, b0, r1, lane, tab, count, 0);
-  }
+  const int count = check ? count_all<true>(a, sc, r0, r1, lane, tab) : count_all<false>(a, sc, r0, r1, lane, tab);
   cnt[lane] = count;
   if (check && __any_sync(kFull, sc.bad) && lane == 0) set_error(a.err, MOE_DEVERR_EXPERT_ID);
   const int below = __reduce_add_sync(kFull, sc.below);
@@ -258,19 +146,7 @@ __global__ void __launch_bounds__(kThreads) lists_kernel(const ListArgs a) {
     a.offsets[sc.e_lo + threadIdx.x] = s_base[threadIdx.x];
 
   // pass 2
-  if (r0 < r1) place_block(a, sc.held, r0, min(kBatch, (r1 - r0 + 31) / 32), sc.nexp, lane, tab, cnt, s_start);
-  for (int b0 = r0 + 32 * kHeld; b0 < r1; b0 += 32 * kBatch) {
-    uint32_t slot[kBatch / 4];
-#pragma unroll
-    for (int h = 0; h < kBatch / 4; ++h) slot[h] = kFull;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = b0 + 32 * u + lane;
-      const unsigned jv = (unsigned)((i < r1 ? __ldg(a.ids + i) : -1) - sc.e_lo);
-      if (jv < (unsigned)sc.nexp) slot[u / 4] &= ~((~jv & 0xFFu) << (8 * (u % 4)));
-    }
-    place_block(a, slot, b0, min(kBatch, (r1 - b0 + 31) / 32), sc.nexp, lane, tab, cnt, s_start);
-  }
+  place_all(a, sc, r0, r1, lane, tab, cnt, s_start);
   cluster_wait();  // no CTA exits while another may still read its shared memory
 }
 

@@ -1,0 +1,222 @@
+// Per-expert routing lists: the per-warp counting and placing steps shared by the
+// cluster kernel of moe_build_routing_lists (lists.cu) and the one-CTA-per-range form
+// that the one-call step runs inside its Finalize launch (finalize.cu).
+//
+// The pair code of ids[t, k] is its flat index i = t*K + k, so for an expert e
+//   offsets[e]             = #{ i : 0 <= ids[i] < e }
+//   pairs[offsets[e] + r]  = the r-th i (ascending) with ids[i] == e
+// i.e. an order-preserving filter of the flat id array. A CTA owns a range of 32
+// experts (one per lane); its warps walk the ids in steps of 32 (lane l reads id
+// step*32 + l: one coalesced 128-byte load per step). Counting and placing use warp
+// votes and single-writer tables only: no atomics.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace lists_impl {
+
+constexpr int kMaxEpc = 32;  // experts per CTA
+constexpr int kBatch = 16;   // steps (32 ids each) in flight per warp
+constexpr int kHeld = 16;    // steps whose owned slots stay in registers
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct ListArgs {
+  const int32_t* ids;
+  int n;  // T * K
+  int E, epc;
+  int32_t* offsets;
+  int32_t* pairs;
+  uint32_t* err;
+};
+
+struct Scan {
+  int e_lo, nexp, n;
+  int below = 0;
+  bool bad = false;
+  uint32_t held[kHeld / 4];  // byte s%4 of held[s/4]: owned slot of step s's id, 0xFF = none
+};
+
+// Pass 1 over kBatch steps from flat id b0 (+ lane); CHECK also flags ids outside [0, E).
+// Within each step the lanes holding an owned expert are grouped by it
+// (__match_any_sync) and the group's lowest lane writes the group size to
+// tab[step][expert] -- one writer per cell, no atomics; lane j then adds column j (its
+// expert) to its count.
+template <bool CHECK, bool HOLD>
+__device__ __forceinline__ void count_batch(const ListArgs& a, Scan& sc, int b0, int r1, int lane,
+                                            uint16_t (*tab)[kMaxEpc], int& count, int step0) {
+  int v[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int i = b0 + 32 * u + lane;
+    v[u] = i < r1 ? __ldg(a.ids + i) : -1;  // -1: never below e_lo, never owned
+    if (CHECK && i < r1 && (unsigned)v[u] >= (unsigned)a.E) sc.bad = true;
+  }
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) tab[u][lane] = 0;
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    sc.below += (unsigned)v[u] < (unsigned)sc.e_lo;
+    const unsigned jv = (unsigned)(v[u] - sc.e_lo);
+    const bool m = jv < (unsigned)sc.nexp;
+    const unsigned bal = __ballot_sync(kFull, m);
+    if (m) {
+      const unsigned peers = __match_any_sync(bal, jv);
+      if ((peers & ((1u << lane) - 1u)) == 0) tab[u][jv] = (uint16_t)__popc(peers);
+      if (HOLD) {
+        const int st = step0 + u;
+        sc.held[st / 4] &= ~((~jv & 0xFFu) << (8 * (st % 4)));
+      }
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) count += tab[u][lane];
+  __syncwarp();
+}
+
+// Pass 2 for one block of up to kBatch steps of a warp: the ids i0 + 32*st + lane, with
+// owned slots in the bytes of slot[] (0xFF = none). (1) Within each step, the matching
+// lanes are grouped by expert (__match_any_sync); a lane's rank is the count of its
+// group's lanes below it, and the group's lowest lane records the group size in
+// tab[st][expert]. The steps do not depend on one another. (2) Lane j turns column j
+// of tab into exclusive prefixes over the steps. (3) Every match is written at
+// base[expert] + run[expert] + tab[st][expert] + rank; lane j then advances run[j].
+__device__ __forceinline__ void place_block(const ListArgs& a, const uint32_t (&slot)[kBatch / 4], int i0, int nsteps,
+                                            int nexp, int lane, uint16_t (*tab)[kMaxEpc], int* run, const int* base) {
+#pragma unroll
+  for (int st = 0; st < kBatch; ++st) tab[st][lane] = 0;
+  __syncwarp();
+  uint32_t rk[kBatch / 4] = {};
+#pragma unroll
+  for (int st = 0; st < kBatch; ++st) {
+    if (st >= nsteps) break;  // warp-uniform
+    const unsigned jv = (slot[st / 4] >> (8 * (st % 4))) & 0xFFu;
+    const bool m = jv < (unsigned)nexp;
+    const unsigned bal = __ballot_sync(kFull, m);
+    if (m) {
+      const unsigned peers = __match_any_sync(bal, jv);
+      const unsigned r = __popc(peers & ((1u << lane) - 1u));
+      rk[st / 4] |= r << (8 * (st % 4));
+      if (r == 0) tab[st][jv] = (uint16_t)__popc(peers);
+    }
+  }
+  __syncwarp();
+  int total = 0;
+#pragma unroll
+  for (int st = 0; st < kBatch; ++st) {
+    const int c = tab[st][lane];
+    tab[st][lane] = (uint16_t)total;
+    total += c;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int st = 0; st < kBatch; ++st) {
+    if (st >= nsteps) break;  // warp-uniform
+    const unsigned jv = (slot[st / 4] >> (8 * (st % 4))) & 0xFFu;
+    if (jv < (unsigned)nexp) {
+      const int r = (int)((rk[st / 4] >> (8 * (st % 4))) & 0xFFu);
+      a.pairs[base[jv] + run[jv] + tab[st][jv] + r] = i0 + 32 * st + lane;
+    }
+  }
+  __syncwarp();
+  run[lane] += total;
+  __syncwarp();
+}
+
+// Pass 2 over the ids [r0, r1) of a warp whose first kHeld steps' owned slots are in
+// sc.held: every match written at base[expert] + run[expert] + its rank in the warp's
+// id order (run[j]: where this warp's share of expert j's list starts, advanced here).
+__device__ __forceinline__ void place_all(const ListArgs& a, const Scan& sc, int r0, int r1, int lane,
+                                          uint16_t (*tab)[kMaxEpc], int* run, const int* base) {
+  if (r0 < r1) place_block(a, sc.held, r0, min(kBatch, (r1 - r0 + 31) / 32), sc.nexp, lane, tab, run, base);
+  for (int b0 = r0 + 32 * kHeld; b0 < r1; b0 += 32 * kBatch) {
+    uint32_t slot[kBatch / 4];
+#pragma unroll
+    for (int h = 0; h < kBatch / 4; ++h) slot[h] = kFull;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = b0 + 32 * u + lane;
+      const unsigned jv = (unsigned)((i < r1 ? __ldg(a.ids + i) : -1) - sc.e_lo);
+      if (jv < (unsigned)sc.nexp) slot[u / 4] &= ~((~jv & 0xFFu) << (8 * (u % 4)));
+    }
+    place_block(a, slot, b0, min(kBatch, (r1 - b0 + 31) / 32), sc.nexp, lane, tab, run, base);
+  }
+}
+
+// Pass 1 over the ids [r0, r1) of a warp: lane j's count of owned expert j (returned),
+// sc.below (this lane's ids below the range) and sc.held filled; CHECK flags ids outside
+// [0, E) in sc.bad.
+template <bool CHECK>
+__device__ __forceinline__ int count_all(const ListArgs& a, Scan& sc, int r0, int r1, int lane,
+                                         uint16_t (*tab)[kMaxEpc]) {
+  int count = 0;
+  if (r0 < r1) count_batch<CHECK, true>(a, sc, r0, r1, lane, tab, count, 0);
+  for (int b0 = r0 + 32 * kHeld; b0 < r1; b0 += 32 * kBatch) count_batch<CHECK, false>(a, sc, b0, r1, lane, tab, count, 0);
+  return count;
+}
+
+// Shared memory of the one-CTA-per-range form (W warps).
+template <int W>
+struct RangeSmem {
+  int cnt[W][kMaxEpc];                    // per (warp, expert): count, then the warp's start in the list
+  __align__(16) uint16_t tab[W][kBatch][kMaxEpc];
+  int below[W];
+  int start[kMaxEpc];                     // where each owned expert's list starts (its offset)
+};
+
+// One CTA of W warps builds the lists of expert range `range` (32 experts) from all
+// the ids, with no other CTA involved: warp w scans the w-th contiguous part of the ids
+// (in steps of 32), the warps' counts are scanned per expert, the ids below the range
+// give the base, and the CTA writes its offsets and places its pairs. Every thread of
+// the CTA calls this; the CTA must already have waited for the ids.
+template <int W>
+__device__ __forceinline__ void lists_range_cta(const ListArgs& a, int range, RangeSmem<W>& sm) {
+  static_assert(W >= 1 && W <= 32, "one warp per part of the ids");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  Scan sc;
+  sc.e_lo = range * kMaxEpc;
+  sc.nexp = min(kMaxEpc, a.E - sc.e_lo);
+  sc.n = a.n;
+#pragma unroll
+  for (int h = 0; h < kHeld / 4; ++h) sc.held[h] = kFull;
+  const int per = ((a.n + 31) / 32 + W - 1) / W * 32;
+  const int r0 = min(a.n, warp * per), r1 = min(a.n, r0 + per);
+  const int count = range == 0 ? count_all<true>(a, sc, r0, r1, lane, sm.tab[warp])
+                               : count_all<false>(a, sc, r0, r1, lane, sm.tab[warp]);
+  sm.cnt[warp][lane] = count;
+  if (range == 0 && __any_sync(kFull, sc.bad) && lane == 0) set_error(a.err, MOE_DEVERR_EXPERT_ID);
+  const int below = __reduce_add_sync(kFull, sc.below);
+  if (lane == 0) sm.below[warp] = below;
+  __syncthreads();
+  if (warp == 0) {
+    // lane j: expert e_lo + j's count over the warps -> each warp's start, the offsets
+    int b = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) b += sm.below[w];
+    int wstart[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      wstart[w] = tot;
+      tot += sm.cnt[w][lane];
+    }
+    int inc = tot;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, d);
+      if (lane >= d) inc += y;
+    }
+    const int off = b + inc - tot;  // offsets[e_lo + lane]
+    sm.start[lane] = off;
+#pragma unroll
+    for (int w = 0; w < W; ++w) sm.cnt[w][lane] = wstart[w];
+    if (lane < sc.nexp) a.offsets[sc.e_lo + lane] = off;
+    if (lane == sc.nexp - 1 && sc.e_lo + sc.nexp == a.E) a.offsets[a.E] = off + tot;
+  }
+  __syncthreads();
+  place_all(a, sc, r0, r1, lane, sm.tab[warp], sm.cnt[warp], sm.start);
+}
+
+}  // namespace lists_impl
+}  // namespace moe

@@ -45,7 +45,11 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
   }
   __syncthreads();  // the barrier is initialised before any thread waits on it
   grid_launch_dependents();
-  if (wait) grid_wait();
+  if (wait) {
+    // the span's DRAM fetch overlaps the preceding kernel's end (a hint only)
+    if (threadIdx.x == 0) prefetch_l2(x + cta0 * 8, (uint32_t)nch * 16u);
+    grid_wait();
+  }
   if (threadIdx.x == 0) {
     mbar_expect_tx(bar, (uint32_t)nch * 16u);
     bulk_g2s(smem_u32(stage), x + cta0 * 8, (uint32_t)nch * 16u, bar, policy_evict_first());
@@ -98,22 +102,22 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
         const int r = (int)(blk / nsc);
         scales[tcgen05_scale_offset(r, (int)(blk - (long long)r * nsc), ct)] = (uint8_t)sbyte;
       }
-      continue;
-    }
-    // scale bytes of the warp's 8 blocks (held by lanes 0, 4, ..., 28)
-    uint32_t b[8];
+    } else {
+      // scale bytes of the warp's 8 blocks (held by lanes 0, 4, ..., 28)
+      uint32_t b[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = __shfl_sync(kFullMask, sbyte, 4 * i);
-    const long long blk0 = (cta0 + wl) >> 2;
-    if (lane == 0) {
-      if (wl + 32 <= nch) {
-        *reinterpret_cast<uint2*>(scales + blk0) =
-            make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
-      } else {
-        const int nb = (nch - wl) >> 2;
+      for (int i = 0; i < 8; ++i) b[i] = __shfl_sync(kFullMask, sbyte, 4 * i);
+      const long long blk0 = (cta0 + wl) >> 2;
+      if (lane == 0) {
+        if (wl + 32 <= nch) {
+          *reinterpret_cast<uint2*>(scales + blk0) = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                                                                b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+        } else {
+          const int nb = (nch - wl) >> 2;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < nb) scales[blk0 + i] = (uint8_t)b[i];
+          for (int i = 0; i < 8; ++i)
+            if (i < nb) scales[blk0 + i] = (uint8_t)b[i];
+        }
       }
     }
   }

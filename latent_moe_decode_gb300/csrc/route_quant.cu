@@ -61,7 +61,8 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   const long long per = (long long)kThreads * kQuantUnroll;
   const long long qblocks = (nchunks + per - 1) / per;
   // (with partials, the warp body also stores the logits as float4)
-  const bool warp = use_warp_body(T, E, part ? static_cast<const void*>(part) : logits, bias) && (!part || aligned(logits, 16));
+  const bool warp = use_warp_body(E, part ? static_cast<const void*>(part) : logits, bias, part ? S : 0) &&
+                    (!part || aligned(logits, 16));
   const long long rblocks = route_blocks(T, warp);
   if (rblocks + qblocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
   DeviceInfo dev;

@@ -6,10 +6,11 @@ namespace {
 
 constexpr int kAlgoAuto = 0, kAlgoSimt = 1, kAlgoTc = 2;
 
+// A handful of tokens: the CUDA-core GEMV (one pass over the gate, no split-K);
+// otherwise the tensor cores.
 int pick(int algo, int T) {
   if (algo != kAlgoAuto) return algo;
-  (void)T;
-  return kAlgoTc;
+  return T <= kGemvMaxTokens ? kAlgoSimt : kAlgoTc;
 }
 
 size_t workspace_for(int T, int H, int E, int sm_count) {
@@ -45,6 +46,7 @@ extern "C" int moe_router_logits_ex(const uint16_t* x, const uint16_t* w, float*
   float* part = static_cast<float*>(workspace);
   cudaStream_t s = as_cuda(stream);
   if (pick(algo, T) == kAlgoSimt) {
+    if (T <= kGemvMaxTokens) return launch_router_gemv(x, w, logits, T, H, E, s);
     int S = 1, kc = 0;
     simt_plan(T, H, E, dev.sm_count, &S, &kc);
     return launch_router_simt(x, w, logits, T, H, E, S, kc, part, s);

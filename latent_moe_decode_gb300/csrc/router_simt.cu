@@ -89,10 +89,13 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
 // read before the wait for the preceding kernel only as a prefetch) so the stream
 // starts while the preceding kernel finishes.
 constexpr int kGemvWarps = 7;
-constexpr int kGemvRows = 2;
-
+// expert rows per CTA: 2 (448 CTAs at E = 896, three resident per SM); 3 at 8 tokens,
+// whose larger register need leaves room for two CTAs per SM (299 CTAs)
 template <int TT>
-__global__ void __launch_bounds__(kGemvWarps * 32) router_gemv_kernel(const uint16_t* __restrict__ x,
+constexpr int gemv_rows() { return TT == 8 ? 3 : 2; }
+
+template <int TT, int kGemvRows = gemv_rows<TT>()>
+__global__ void __launch_bounds__(kGemvWarps * 32, TT == 8 ? 2 : 3) router_gemv_kernel(const uint16_t* __restrict__ x,
                                                                       const uint16_t* __restrict__ w,
                                                                       float* __restrict__ out, int T, int H, int E) {
   __shared__ float red[kGemvWarps][kGemvRows * TT];
@@ -116,25 +119,34 @@ __global__ void __launch_bounds__(kGemvWarps * 32) router_gemv_kernel(const uint
   for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
-#pragma unroll(TT <= 2 ? 4 : 2)
-  for (int i = 0; i < NI; ++i) {
-    const int f = lane + 32 * (warp + kGemvWarps * i);
-    if (f >= F) break;
-    uint4 wv[kGemvRows], xv[TT];
+  // NU fragments per lane at a time: all their loads first (addresses clamped into the
+  // row, contributions past the row dropped), then the products in hidden order
+  constexpr int NU = TT <= 4 ? 4 : 2;
+  for (int i0 = 0; i0 < NI; i0 += NU) {
+    uint4 wv[NU][kGemvRows], xv[NU][TT];
 #pragma unroll
-    for (int r = 0; r < kGemvRows; ++r) wv[r] = ld_nc16(wr[r] + f * 8);
+    for (int u = 0; u < NU; ++u) {
+      const int f = min(lane + 32 * (warp + kGemvWarps * (i0 + u)), F - 1);
 #pragma unroll
-    for (int t = 0; t < TT; ++t) xv[t] = t < T ? ld_nc16(x + (size_t)t * H + f * 8) : make_uint4(0, 0, 0, 0);
+      for (int r = 0; r < kGemvRows; ++r) wv[u][r] = ld_nc16(wr[r] + f * 8);
 #pragma unroll
-    for (int r = 0; r < kGemvRows; ++r) {
-      const uint32_t a4[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+      for (int t = 0; t < TT; ++t) xv[u][t] = ld_nc16(x + (size_t)min(t, T - 1) * H + f * 8);
+    }
 #pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const uint32_t b4[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+    for (int u = 0; u < NU; ++u) {
+      const int f = lane + 32 * (warp + kGemvWarps * (i0 + u));
+      if (i0 + u >= NI || f >= F) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[r][t] = __fmaf_rn(bf16_lo(a4[j]), bf16_lo(b4[j]), acc[r][t]);
-          acc[r][t] = __fmaf_rn(bf16_hi(a4[j]), bf16_hi(b4[j]), acc[r][t]);
+      for (int r = 0; r < kGemvRows; ++r) {
+        const uint32_t a4[4] = {wv[u][r].x, wv[u][r].y, wv[u][r].z, wv[u][r].w};
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const uint32_t b4[4] = {xv[u][t].x, xv[u][t].y, xv[u][t].z, xv[u][t].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[r][t] = __fmaf_rn(bf16_lo(a4[j]), bf16_lo(b4[j]), acc[r][t]);
+            acc[r][t] = __fmaf_rn(bf16_hi(a4[j]), bf16_hi(b4[j]), acc[r][t]);
+          }
         }
       }
     }
@@ -196,12 +208,17 @@ int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int 
   return launch_router_reduce(part, S, T, E, logits, stream);
 }
 
+template <int TT>
+int launch_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, cudaStream_t stream) {
+  const dim3 grid((E + gemv_rows<TT>() - 1) / gemv_rows<TT>()), block(kGemvWarps * 32);
+  return launch_pdl(router_gemv_kernel<TT>, grid, block, 0, stream, x, w, logits, T, H, E);
+}
+
 int launch_router_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, cudaStream_t stream) {
-  const dim3 grid((E + kGemvRows - 1) / kGemvRows), block(kGemvWarps * 32);
-  if (T <= 1) return launch_pdl(router_gemv_kernel<1>, grid, block, 0, stream, x, w, logits, T, H, E);
-  if (T <= 2) return launch_pdl(router_gemv_kernel<2>, grid, block, 0, stream, x, w, logits, T, H, E);
-  if (T <= 4) return launch_pdl(router_gemv_kernel<4>, grid, block, 0, stream, x, w, logits, T, H, E);
-  if (T <= kGemvMaxTokens) return launch_pdl(router_gemv_kernel<8>, grid, block, 0, stream, x, w, logits, T, H, E);
+  if (T <= 1) return launch_gemv<1>(x, w, logits, T, H, E, stream);
+  if (T <= 2) return launch_gemv<2>(x, w, logits, T, H, E, stream);
+  if (T <= 4) return launch_gemv<4>(x, w, logits, T, H, E, stream);
+  if (T <= kGemvMaxTokens) return launch_gemv<8>(x, w, logits, T, H, E, stream);
   return MOE_ERR_INVALID_ARGUMENT;
 }
 

@@ -717,6 +717,10 @@ int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T,
 // are written to `logits` directly and *S_out = 1; otherwise *S_out = S.
 int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int sm_count,
                            float* part, uint32_t* err, cudaStream_t stream, int* S_out) {
+  if (T <= kGemvMaxTokens) {  // what moe_router_logits runs for a handful of tokens
+    *S_out = 1;
+    return launch_router_gemv(x, w, logits, T, H, E, stream);
+  }
   TcPlan p = tc_plan(T, H, E, sm_count);
   if (p.S == 1 || p.bn <= 64) {
     *S_out = 1;
@@ -746,6 +750,7 @@ int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, 
 }
 
 size_t router_partials_bytes(int T, int H, int E, int sm_count) {
+  if (T <= kGemvMaxTokens) return 0;
   const TcPlan p = tc_plan(T, H, E, sm_count);
   return (p.S > 1 && p.bn > 64) ? (size_t)p.S * T * E * sizeof(float) : 0;
 }

@@ -55,7 +55,7 @@ extern "C" int moe_topk_route(const float* logits, const float* bias, int T, int
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   TopkArgs a{logits, bias, T, E, K, renormalize ? 1 : 0, scale, ids, weights, weights_bf16};
-  const bool warp = use_warp_body(T, E, logits, bias);
+  const bool warp = use_warp_body(E, logits, bias);
   const dim3 grid((unsigned)route_blocks(T, warp)), block(kThreads);
   cudaStream_t s = as_cuda(stream);
   if (E > kWarpMaxE) return launch_pdl(topk_kernel<32, false>, grid, block, 0, s, a);

@@ -104,7 +104,8 @@ struct TopkArgs {
 
 constexpr int kThreads = 128;  // both bodies: CTAs of 4 warps
 constexpr int kWarps = kThreads / 32;
-constexpr int kWarpMaxE = 1024;  // the warp body's experts (32 per lane at most)
+constexpr int kWarpMaxE = 1024;     // the warp body's experts (32 per lane at most)
+constexpr int kMaxPartSplits = 8;  // split-K partials the warp body sums (wide token tiles split at most 8 ways)
 
 // The logits of this thread's experts e = e_first + e_stride * j (j < NJ; a warp's 32
 // lanes cover one 128-byte line per j). PART: the sum in split order of the router's S
@@ -232,29 +233,24 @@ template <int NJ4, bool PART>
 __device__ __forceinline__ void load_logits4(const TopkArgs& a, int t, float4 (&x)[NJ4]) {
   const int lane = threadIdx.x & 31, E = a.E;
   if constexpr (PART) {
-    for (int s0 = 0; s0 < a.S; s0 += 2) {
-      const float* r0 = a.part + ((size_t)s0 * a.T + t) * E;
-      const float* r1 = r0 + (size_t)a.T * E;
-      const bool two = s0 + 1 < a.S;
-      float4 p0[NJ4], p1[NJ4];
+    // group j: every split's float4 loaded at once (up to kMaxPartSplits), then summed
+    // in split order; the groups are independent, so several are in flight together
+    const float* base = a.part + (size_t)t * E + 4 * lane;
+    const size_t sstride = (size_t)a.T * E;
 #pragma unroll
-      for (int j = 0; j < NJ4; ++j) {
-        const int e = 128 * j + 4 * lane;
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        p0[j] = e < E ? __ldcg(reinterpret_cast<const float4*>(r0 + e)) : z;
-        p1[j] = (two && e < E) ? __ldcg(reinterpret_cast<const float4*>(r1 + e)) : z;
-      }
+    for (int j = 0; j < NJ4; ++j) {
+      const bool in = 128 * j + 4 * lane < E;
+      float4 p[kMaxPartSplits];
 #pragma unroll
-      for (int j = 0; j < NJ4; ++j) {
-        if (s0 == 0) {
-          x[j] = p0[j];
-        } else {
-          x[j].x = __fadd_rn(x[j].x, p0[j].x), x[j].y = __fadd_rn(x[j].y, p0[j].y);
-          x[j].z = __fadd_rn(x[j].z, p0[j].z), x[j].w = __fadd_rn(x[j].w, p0[j].w);
-        }
-        if (two) {
-          x[j].x = __fadd_rn(x[j].x, p1[j].x), x[j].y = __fadd_rn(x[j].y, p1[j].y);
-          x[j].z = __fadd_rn(x[j].z, p1[j].z), x[j].w = __fadd_rn(x[j].w, p1[j].w);
+      for (int q = 0; q < kMaxPartSplits; ++q)
+        p[q] = (in && q < a.S) ? __ldcg(reinterpret_cast<const float4*>(base + q * sstride + 128 * j))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[j] = p[0];
+#pragma unroll
+      for (int q = 1; q < kMaxPartSplits; ++q) {
+        if (q < a.S) {
+          x[j].x = __fadd_rn(x[j].x, p[q].x), x[j].y = __fadd_rn(x[j].y, p[q].y);
+          x[j].z = __fadd_rn(x[j].z, p[q].z), x[j].w = __fadd_rn(x[j].w, p[q].w);
         }
       }
     }
@@ -616,6 +612,12 @@ __device__ __forceinline__ void topk_token_cta(const TopkArgs& a, const int t) {
 template <int NJ, bool WARP, bool PART>
 __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
   grid_launch_dependents();
+  if (!PART && (a.E & 3) == 0) {
+    // the logits rows' DRAM fetch overlaps the preceding kernel's end (a hint only)
+    const int t = WARP ? blk * kWarps + (int)(threadIdx.x >> 5) : blk;
+    if ((threadIdx.x & (WARP ? 31 : 127)) == 0 && t < a.T && aligned(a.logits, 16))
+      prefetch_l2(a.logits + (size_t)t * a.E, (uint32_t)a.E * 4u);
+  }
   grid_wait();
   if constexpr (WARP) {
     __shared__ WarpScratch ws[kWarps];
@@ -629,13 +631,11 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
 // Routing CTAs for T tokens.
 __host__ __device__ constexpr int route_blocks(int T, bool warp) { return warp ? (T + kWarps - 1) / kWarps : T; }
 
-// Which body routes a launch. A token's four warps (CTA body) finish it sooner than one
-// warp does, so the CTA body takes small batches; from kWarpMinTokens tokens on the
-// warp body (a quarter of the instructions per token, no CTA barrier) does, when its
-// float4 layout applies: E <= kWarpMaxE, E % 4 == 0, 16-byte aligned rows and bias.
-constexpr int kWarpMinTokens = 192;
-inline bool use_warp_body(int T, int E, const void* rows, const float* bias) {
-  return T >= kWarpMinTokens && E <= kWarpMaxE && E % 4 == 0 && aligned(rows, 16) && (!bias || aligned(bias, 16));
+// Which body routes a launch: the warp body (measured faster at every batch size, 1 to
+// 4096 tokens) wherever its float4 layout applies -- E <= kWarpMaxE, E % 4 == 0,
+// 16-byte aligned rows and bias, at most kMaxPartSplits partials -- else the CTA body.
+inline bool use_warp_body(int E, const void* rows, const float* bias, int S = 0) {
+  return E <= kWarpMaxE && E % 4 == 0 && aligned(rows, 16) && (!bias || aligned(bias, 16)) && S <= kMaxPartSplits;
 }
 
 }  // namespace topk_impl

@@ -95,3 +95,32 @@ def test_one_call_equals_four_calls(moe, T):
                     ("pairs", pairs), ("q", q), ("scales", sc), ("out", out)):
         a = getattr(one, name)
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name
+
+
+@pytest.mark.parametrize("T,H,L,E,K", [(37, 512, 256, 100, 8), (300, 1024, 512, 1000, 16), (9, 256, 64, 40, 3),
+                                       (130, 768, 128, 2048, 16)])
+def test_one_call_other_shapes(moe, orc, T, H, L, E, K):
+    """The one-call step at shapes other than the decode layer's -- a last expert range
+    of the lists shorter than 32 experts, K of 8, 3 and 16, E up to 2048 (the CTA-per-
+    token top-K) -- equals the four calls bit for bit, and its lists the oracle's."""
+    x = synth.normal_bf16(50 + T, 1, (T, H))
+    w = synth.normal_bf16(50 + E, 2, (E, H), 0.02)
+    bias = synth.normal_f32(50 + E, 3, (E,), 0.01)
+    latent = synth.normal_bf16(50 + T, 5, (T, L))
+    rows = synth.normal_bf16(50 + T, 4, (T * K, L))
+    xd, wd, bd, ld, rd = bf16_dev(x), bf16_dev(w), dev(bias), bf16_dev(latent), bf16_dev(rows)
+    one = moe.RouteFinalize(T, H, L, E, K)
+    one.run(xd, wd, bd, ld, rd)
+    logits = moe.router_logits(xd, wd)
+    ids, wf, wb, q, sc = moe.topk_route_quantize(logits, bd, K, ld)
+    off, pairs = moe.build_routing_lists(ids, E)
+    out = moe.finalize(rd, wb, T, K)
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 0
+    for name, b in (("logits", logits), ("ids", ids), ("weights", wf), ("weights_bf16", wb), ("offsets", off),
+                    ("pairs", pairs), ("q", q), ("scales", sc), ("out", out)):
+        a = getattr(one, name)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name
+    eoff, epairs = orc.routing_lists(host(one.ids), E)
+    np.testing.assert_array_equal(host(one.offsets), eoff)
+    np.testing.assert_array_equal(host(one.pairs), epairs)

@@ -19,7 +19,8 @@ def _ints(seed, shape, lo=-8, hi=8):
 
 
 @pytest.mark.parametrize("algo", list(ALGOS))
-@pytest.mark.parametrize("T,E,H", [(1, 896, 7168), (8, 896, 7168), (17, 128, 1024), (64, 896, 7168), (100, 200, 512),
+@pytest.mark.parametrize("T,E,H", [(1, 896, 7168), (2, 896, 7168), (3, 896, 7168), (5, 896, 7168), (8, 896, 7168),
+                                   (4, 7, 72), (6, 1001, 232), (17, 128, 1024), (64, 896, 7168), (100, 200, 512),
                                    (300, 896, 1024), (1020, 256, 7168),
                                    # plan branches at the full gate: 64-column tiles (T = 128), 128-column
                                    # tiles (T = 256); CTA pairs with a padding half and a split (T = 2048)
