@@ -389,16 +389,19 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  * i.e. Finalize combines the expanded expert rows (row t*K + k = token t's k-th
  * expert) with the BF16 routing weights, as the wide page's Finalize does. Every
  * output equals the four calls' bit for bit. It takes three launches (programmatic
- * dependent launch between them): the router; top-K with the MXFP8 of the latent; and
- * Finalize, whose launch also builds the routing lists in CTAs of its own (Finalize
- * does not read them, so they are built beside its row stream). For token tiles wider
+ * dependent launch between them): the router; top-K with the MXFP8 of the latent, whose
+ * routing CTAs (four tokens each) also write each token's slots by expert to the
+ * workspace; and Finalize, whose launch also builds the routing lists from those slots
+ * in CTAs of its own (Finalize does not read the lists, so they are built beside its row
+ * stream). Where top-K runs one CTA per token (E > 1024 or E % 4 != 0) the lists kernel
+ * runs between the last two launches instead. For token tiles wider
  * than 64 the router stores its split-K partials in the workspace instead of reducing
  * them, and the top-K launch sums each token's partials in the same split order before
  * selecting: the same logits, one on-chip exchange fewer. Arguments, layouts and
  * requirements are those of the four calls (weights may be NULL; weights_bf16 may
  * not); they are all checked before the first launch. `workspace` holds
- * moe_route_finalize_workspace(T, H, E, K) bytes (NULL when that is 0); it is
- * clobbered. Returns the first non-OK status (nothing is launched after it). Allocates
+ * moe_route_finalize_workspace(T, H, E, K) bytes, 16-byte aligned (the router's
+ * split-K partials and the top-K launch's slot map for the lists); it is clobbered. Returns the first non-OK status (nothing is launched after it). Allocates
  * nothing, so the call can be captured in a CUDA graph.
  * ------------------------------------------------------------------------------- */
 size_t moe_route_finalize_workspace(int T, int H, int E, int K);

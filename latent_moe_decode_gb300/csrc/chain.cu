@@ -12,18 +12,26 @@
 #include "router.cuh"
 
 namespace {
-// the router's partials [S][T][E] (or its cluster workspace, if larger), then the lists'
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// the router's partials [S][T][E] (or its cluster workspace, if larger)
 size_t router_part_bytes(int T, int H, int E) {
   moe::DeviceInfo dev;
   if (T < 1 || H < 8 || E < 1 || moe::current_device(&dev) != MOE_OK) return 0;
   const size_t a = moe_router_logits_workspace(T, H, E), b = moe::router_partials_bytes(T, H, E, dev.sm_count);
-  const size_t n = a > b ? a : b;
-  return (n + 255) / 256 * 256;
+  return align256(a > b ? a : b);
+}
+
+// the routing CTAs' slot map [ceil(T/4)][E] words and range counts [ceil(T/4)][ceil(E/32)]
+size_t map_bytes(int T, int E) {
+  if (T < 1 || E < 1) return 0;
+  const size_t nb = (size_t)(T + 3) / 4;
+  return align256(nb * E * 4) + align256(nb * ((E + 31) / 32));
 }
 }  // namespace
 
 extern "C" size_t moe_route_finalize_workspace(int T, int H, int E, int K) {
-  return router_part_bytes(T, H, E) + moe_build_routing_lists_workspace(T, K, E);
+  return router_part_bytes(T, H, E) + map_bytes(T, E) + moe_build_routing_lists_workspace(T, K, E);
 }
 
 extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const float* bias, const uint16_t* latent,
@@ -39,10 +47,10 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(logits, 4)) return MOE_ERR_ALIGNMENT;
   if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(offsets, 4) || !aligned(pairs, 4))
     return MOE_ERR_ALIGNMENT;
-  const size_t rws = router_part_bytes(T, H, E);
+  const size_t rws = router_part_bytes(T, H, E), mws = map_bytes(T, E);
   const size_t lws = moe_build_routing_lists_workspace(T, K, E);
-  if (workspace_bytes < rws + lws || (rws + lws > 0 && !workspace)) return MOE_ERR_WORKSPACE;
-  if (rws > 0 && !aligned(workspace, 16)) return MOE_ERR_WORKSPACE;
+  if (workspace_bytes < rws + mws + lws || !workspace) return MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return MOE_ERR_WORKSPACE;
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
@@ -55,13 +63,22 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   st = launch_router_partials(x, w, logits, T, H, E, dev.sm_count, part, dev.error_word, as_cuda(stream), &S);
   if (st != MOE_OK) return st;
   // the latent is an input of the step, complete before the router started: the
-  // quantisation CTAs run beside the router instead of after it
+  // quantisation CTAs run beside the router instead of after it. The routing CTAs also
+  // write a slot map from which the Finalize launch builds the routing lists in CTAs of
+  // its own, beside its row stream (Finalize does not read the lists); where the
+  // warp-per-token body does not apply, the lists kernel runs between the two.
+  const float* pp = S > 1 ? part : nullptr;
+  const bool map = route_uses_warp_body(E, logits, bias, pp, S);
+  uint32_t* smap = reinterpret_cast<uint32_t*>(ws + rws);
+  uint8_t* rcount = ws + rws + align256((size_t)(T + 3) / 4 * E * 4);
   st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
-                      true, as_cuda(stream), S > 1 ? part : nullptr, S);
+                      true, as_cuda(stream), pp, S, map ? smap : nullptr, map ? rcount : nullptr);
   if (st != MOE_OK) return st;
   // Finalize starts its row copies (a step input) before its wait and reads top-K's
-  // weights after it; the same launch builds the routing lists of top-K's ids in CTAs
-  // of its own (one per 32 experts), beside the row stream, so the lists cost the step
-  // no launch and no time on its critical path.
-  return moe::finalize_with_lists(rows, weights_bf16, T, K, L, out, ids, E, offsets, pairs, moe::as_cuda(stream));
+  // weights after it.
+  if (map) return finalize_with_lists(rows, weights_bf16, T, K, L, out, smap, rcount, E, offsets, pairs, as_cuda(stream));
+  st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws + mws : nullptr, lws, stream);
+  if (st != MOE_OK) return st;
+  return finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out, true,
+                  as_cuda(stream));
 }

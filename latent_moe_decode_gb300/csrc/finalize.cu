@@ -49,9 +49,9 @@ struct FinArgs {
   // shared rows) were complete before the preceding kernel started, so the first row
   // copies are issued before the wait, and the weights (and indices) after it
   int wait_all;
-  // LISTS instantiations: the first n_list CTAs build the routing lists of la (one
-  // 32-expert range each) instead of summing rows
-  lists_impl::ListArgs la;
+  // LISTS instantiations: the first n_list CTAs build the routing lists from the
+  // routing CTAs' slot map (one 32-expert range each) instead of summing rows
+  lists_impl::MapArgs lm;
   int n_list;
 };
 
@@ -77,9 +77,8 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   if constexpr (LISTS) {
     if (cta < a.n_list) {
       grid_launch_dependents();
-      grid_wait();  // the ids come from the preceding kernel
-      lists_impl::lists_range_cta<kThreads / 32>(a.la, cta,
-                                                 *reinterpret_cast<lists_impl::RangeSmem<kThreads / 32>*>(slots));
+      grid_wait();  // the slot map comes from the preceding kernel
+      lists_impl::lists_from_map<kThreads / 32>(a.lm, cta, *reinterpret_cast<lists_impl::MapSmem<kThreads / 32>*>(slots));
       return;
     }
     cta -= a.n_list;
@@ -232,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
 template <int KT, bool G, bool B, bool S, bool LISTS = false>
 int launch_one(const FinArgs& a, int sm_count, cudaStream_t s) {
   size_t smem = (size_t)kStages * ((KT ? KT : a.K) + (S ? 1 : 0)) * kThreads * 16;
-  if (LISTS && smem < sizeof(lists_impl::RangeSmem<kThreads / 32>)) smem = sizeof(lists_impl::RangeSmem<kThreads / 32>);
+  if (LISTS && smem < sizeof(lists_impl::MapSmem<kThreads / 32>)) smem = sizeof(lists_impl::MapSmem<kThreads / 32>);
   auto kern = finalize_kernel<KT, G, B, S, LISTS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
   int per_sm = 0;
@@ -294,22 +293,24 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
 }
 
 // Finalize of the one-call step (rows t*K + k, BF16 weights; rows ready before the
-// preceding kernel started) with the routing lists of `ids` built by the same launch.
+// preceding kernel started) with the routing lists built by the same launch from the
+// routing CTAs' slot map.
 int finalize_with_lists(const uint16_t* rows, const uint16_t* weights_bf16, int T, int K, int H, uint16_t* out,
-                        const int32_t* ids, int E, int32_t* offsets, int32_t* pairs, cudaStream_t s) {
+                        const uint32_t* smap, const uint8_t* rcount, int E, int32_t* offsets, int32_t* pairs,
+                        cudaStream_t s) {
   if (T < 1 || K < 1 || K > MOE_MAX_TOPK || H < 8 || H % 8 != 0 || E < 1 || E > MOE_MAX_EXPERTS)
     return MOE_ERR_INVALID_ARGUMENT;
   if ((long long)T * K > (1LL << 31) - 1 || (long long)T * (H / 8) > (1LL << 31) * (long long)kThreads - 1)
     return MOE_ERR_CAPACITY;
-  if (!rows || !weights_bf16 || !out || !ids || !offsets || !pairs) return MOE_ERR_INVALID_ARGUMENT;
-  if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(weights_bf16, 2) || !aligned(ids, 4) ||
+  if (!rows || !weights_bf16 || !out || !smap || !rcount || !offsets || !pairs) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(weights_bf16, 2) || !aligned(smap, 4) ||
       !aligned(offsets, 4) || !aligned(pairs, 4))
     return MOE_ERR_ALIGNMENT;
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   FinArgs a{rows, (long long)T * K, nullptr, weights_bf16, nullptr, 1.0f, T, K, H, out, dev.error_word, 0};
-  a.la = lists_impl::ListArgs{ids, T * K, E, lists_impl::kMaxEpc, offsets, pairs, dev.error_word};
+  a.lm = lists_impl::MapArgs{smap, rcount, T, K, E, offsets, pairs};
   a.n_list = (E + lists_impl::kMaxEpc - 1) / lists_impl::kMaxEpc;
   if (K == 16) return launch_one<16, false, true, false, true>(a, dev.sm_count, s);
   if (K == 8) return launch_one<8, false, true, false, true>(a, dev.sm_count, s);

@@ -218,5 +218,97 @@ __device__ __forceinline__ void lists_range_cta(const ListArgs& a, int range, Ra
   place_all(a, sc, r0, r1, lane, sm.tab[warp], sm.cnt[warp], sm.start);
 }
 
+// ---------------------------------------------------------------------------------
+// The one-call step's lists from the routing CTAs' slot map (TopkArgs::smap): the map
+// holds, for every 4-token block b and expert e, the four tokens' slots of e (0xFF when
+// absent), so expert e's list is the present bytes of column e in (b, byte) order --
+// token order -- and its pair codes are (4b + i) * K + slot. One CTA of W warps builds
+// the lists of one range of 32 experts (lane = expert): warp w takes a contiguous share
+// of the blocks; pass 1 counts each expert's pairs in the share, the shares' counts are
+// scanned per expert and the range's totals over the experts, the lower ranges' pair
+// counts (rcount) give the base, and pass 2 writes every pair in order. No atomics.
+struct MapArgs {
+  const uint32_t* smap;   // [nb][E]
+  const uint8_t* rcount;  // [nb][ceil(E / 32)]
+  int T, K, E;
+  int32_t* offsets;
+  int32_t* pairs;
+};
+
+template <int W>
+struct MapSmem {
+  int cnt[W][kMaxEpc];  // per (warp, expert): pairs in the warp's share, then where they start
+  int base[W];
+};
+
+constexpr int kMapUnroll = 16;  // map words in flight per lane
+
+template <int W>
+__device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapSmem<W>& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nb = (m.T + 3) / 4, nr = (m.E + 31) / 32;
+  const int e = range * kMaxEpc + lane;
+  const bool ev = e < m.E;
+  // the pairs of the lower ranges
+  int lower = 0;
+  for (int i = threadIdx.x; i < nb * range; i += W * 32) {
+    const int b = i / range;
+    lower += m.rcount[(size_t)b * nr + (i - b * range)];
+  }
+  lower = __reduce_add_sync(kFull, lower);
+  if (lane == 0) sm.base[warp] = lower;
+  const int per = (nb + W - 1) / W, b0 = min(nb, warp * per), b1 = min(nb, b0 + per);
+  const uint32_t* col = m.smap + e;
+  // pass 1: expert e's pairs in this warp's blocks
+  int c = 0;
+  for (int b = b0; b < b1; b += kMapUnroll) {
+    uint32_t wv[kMapUnroll];
+#pragma unroll
+    for (int u = 0; u < kMapUnroll; ++u) wv[u] = (ev && b + u < b1) ? __ldcg(col + (size_t)(b + u) * m.E) : 0xFFFFFFFFu;
+#pragma unroll
+    for (int u = 0; u < kMapUnroll; ++u) c += __popc(~wv[u] & 0x80808080u);
+  }
+  sm.cnt[warp][lane] = c;
+  __syncthreads();
+  if (warp == 0) {
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) base += sm.base[w];
+    int wstart[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      wstart[w] = tot;
+      tot += sm.cnt[w][lane];
+    }
+    int inc = tot;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, d);
+      if (lane >= d) inc += y;
+    }
+    const int off = base + inc - tot;
+#pragma unroll
+    for (int w = 0; w < W; ++w) sm.cnt[w][lane] = off + wstart[w];
+    if (ev) m.offsets[e] = off;
+    if (e == m.E - 1) m.offsets[m.E] = off + tot;
+  }
+  __syncthreads();
+  // pass 2: the pairs of expert e in this warp's blocks, in token order
+  int pos = sm.cnt[warp][lane];
+  for (int b = b0; b < b1; b += kMapUnroll) {
+    uint32_t wv[kMapUnroll];
+#pragma unroll
+    for (int u = 0; u < kMapUnroll; ++u) wv[u] = (ev && b + u < b1) ? __ldcg(col + (size_t)(b + u) * m.E) : 0xFFFFFFFFu;
+#pragma unroll
+    for (int u = 0; u < kMapUnroll; ++u) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t slot = (wv[u] >> (8 * i)) & 0xFFu;
+        if (slot != 0xFFu) m.pairs[pos++] = (4 * (b + u) + i) * m.K + (int)slot;
+      }
+    }
+  }
+}
+
 }  // namespace lists_impl
 }  // namespace moe

@@ -89,13 +89,14 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
 // read before the wait for the preceding kernel only as a prefetch) so the stream
 // starts while the preceding kernel finishes.
 constexpr int kGemvWarps = 7;
-// expert rows per CTA: 2 (448 CTAs at E = 896, three resident per SM); 3 at 8 tokens,
-// whose larger register need leaves room for two CTAs per SM (299 CTAs)
+// expert rows per CTA: 2 (448 CTAs at E = 896, three resident per SM); 6 at 8 tokens
+// (150 CTAs, one per SM): the tokens' rows are re-read from L2 by every CTA, so fewer,
+// wider CTAs read them fewer times
 template <int TT>
-constexpr int gemv_rows() { return TT == 8 ? 3 : 2; }
+constexpr int gemv_rows() { return TT == 8 ? 6 : 2; }
 
 template <int TT, int kGemvRows = gemv_rows<TT>()>
-__global__ void __launch_bounds__(kGemvWarps * 32, TT == 8 ? 2 : 3) router_gemv_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kGemvWarps * 32, TT == 8 ? 1 : 3) router_gemv_kernel(const uint16_t* __restrict__ x,
                                                                       const uint16_t* __restrict__ w,
                                                                       float* __restrict__ out, int T, int H, int E) {
   __shared__ float red[kGemvWarps][kGemvRows * TT];

@@ -100,6 +100,12 @@ struct TopkArgs {
   int S = 0;
   float* logits_out = nullptr;
   int discard = 0;
+  // Optional (warp body): each 4-token routing CTA b also writes, for the routing lists
+  // that the one-call step builds in its Finalize launch, smap[b][e] (byte i: the slot
+  // of expert e in token 4b + i, 0xFF when that token did not pick e) and
+  // rcount[b][r] (its pairs with an expert in range r of 32 experts).
+  uint32_t* smap = nullptr;
+  uint8_t* rcount = nullptr;
 };
 
 constexpr int kThreads = 128;  // both bodies: CTAs of 4 warps
@@ -621,8 +627,25 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
   grid_wait();
   if constexpr (WARP) {
     __shared__ WarpScratch ws[kWarps];
-    const int warp = threadIdx.x >> 5, t = blk * kWarps + warp;
+    __shared__ uint32_t s_map[kWarpMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = blk * kWarps + warp;
+    if (a.smap)
+      for (int i = threadIdx.x; i < a.E; i += kThreads) s_map[i] = 0xFFFFFFFFu;
     if (t < a.T) topk_token_warp<NJ, PART>(a, t, ws[warp]);
+    if (a.smap) {
+      __syncthreads();  // the map is cleared and every token's slots are known
+      // byte `warp` of expert e's word: this token's slot of e (a token's experts are
+      // distinct, so every byte has one writer)
+      if (t < a.T && lane < a.K) reinterpret_cast<uint8_t*>(s_map)[4 * ws[warp].slot_id[lane] + warp] = (uint8_t)lane;
+      __syncthreads();
+      const int nr = (a.E + 31) / 32;
+      for (int r = threadIdx.x; r < nr; r += kThreads) {
+        int c = 0;  // slot bytes are below 0x80, absent ones 0xFF
+        for (int e = 32 * r; e < min(a.E, 32 * r + 32); ++e) c += __popc(~s_map[e] & 0x80808080u);
+        a.rcount[(size_t)blk * nr + r] = (uint8_t)c;
+      }
+      for (int i = threadIdx.x; i < a.E; i += kThreads) a.smap[(size_t)blk * a.E + i] = s_map[i];
+    }
   } else {
     topk_token_cta<NJ, PART>(a, blk);
   }
