@@ -22,11 +22,12 @@ size_t router_part_bytes(int T, int H, int E) {
   return align256(a > b ? a : b);
 }
 
-// the routing CTAs' slot map [ceil(T/4)][E] words and range counts [ceil(T/4)][ceil(E/32)]
+// the routing CTAs' slot map [ceil(E/32)][nb][32] words (nb = ceil(T/4) blocks of 4
+// tokens) and its below counts [ceil(E/32)][nb rounded up to 16] bytes
+size_t smap_bytes(int T, int E) { return align256((size_t)(E + 31) / 32 * ((T + 3) / 4) * 32 * 4); }
 size_t map_bytes(int T, int E) {
   if (T < 1 || E < 1) return 0;
-  const size_t nb = (size_t)(T + 3) / 4;
-  return align256(nb * E * 4) + align256(nb * ((E + 31) / 32));
+  return smap_bytes(T, E) + align256((size_t)(E + 31) / 32 * (((T + 3) / 4 + 15) / 16 * 16));
 }
 }  // namespace
 
@@ -70,13 +71,13 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   const float* pp = S > 1 ? part : nullptr;
   const bool map = route_uses_warp_body(E, logits, bias, pp, S);
   uint32_t* smap = reinterpret_cast<uint32_t*>(ws + rws);
-  uint8_t* rcount = ws + rws + align256((size_t)(T + 3) / 4 * E * 4);
+  uint8_t* below = ws + rws + smap_bytes(T, E);
   st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
-                      true, as_cuda(stream), pp, S, map ? smap : nullptr, map ? rcount : nullptr);
+                      true, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr);
   if (st != MOE_OK) return st;
   // Finalize starts its row copies (a step input) before its wait and reads top-K's
   // weights after it.
-  if (map) return finalize_with_lists(rows, weights_bf16, T, K, L, out, smap, rcount, E, offsets, pairs, as_cuda(stream));
+  if (map) return finalize_with_lists(rows, weights_bf16, T, K, L, out, smap, below, E, offsets, pairs, as_cuda(stream));
   st = moe_build_routing_lists(ids, T, K, E, offsets, pairs, lws ? ws + rws + mws : nullptr, lws, stream);
   if (st != MOE_OK) return st;
   return finalize(rows, (int64_t)T * K, nullptr, weights_bf16, MOE_DTYPE_BF16, nullptr, 1.0f, T, K, L, out, true,

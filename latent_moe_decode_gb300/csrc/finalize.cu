@@ -94,15 +94,23 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   grid_launch_dependents();
   // indices choose the rows to copy: with a gather, everything waits
   const bool early = !a.wait_all && !GATHER;
-  if (!GATHER && !early && threadIdx.x < K) {
-    // the CTA's first fragments (128 consecutive ones, at most two tokens) of row k:
-    // their DRAM fetch overlaps the preceding kernel's end (a hint only)
+  if (!early && threadIdx.x < 32) {
+    // The CTA's first fragments (128 consecutive ones, at most two tokens): the row
+    // spans (without a gather), the shared-row spans, and the tokens' indices and weights
+    // are asked of L2 before the wait, so their DRAM fetch overlaps the preceding
+    // kernel's end (hints only: nothing is read into registers or shared memory).
+    const int lane = threadIdx.x;
     const long long lo = (long long)cta * kThreads, hi = min(lo + kThreads, total);
     for (long long f = lo; f < hi;) {
       const int t = (int)(f / frags);
       const long long end = min(hi, (long long)(t + 1) * frags);
-      prefetch_l2(a.rows + ((size_t)t * K + threadIdx.x) * a.H + (size_t)(f - (long long)t * frags) * 8,
-                  (uint32_t)(end - f) * 16u);
+      const size_t col = (size_t)(f - (long long)t * frags) * 8;
+      const uint32_t bytes = (uint32_t)(end - f) * 16u;
+      if (!GATHER)
+        for (int k = lane; k < K; k += 32) prefetch_l2(a.rows + ((size_t)t * K + k) * a.H + col, bytes);
+      if (SHARED && lane == 0) prefetch_l2(a.shared + (size_t)t * a.H + col, bytes);
+      if (GATHER && lane == 1) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.row_index + (size_t)t * K));
+      if (lane == 2) asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(a.weights) + (size_t)t * K * (BF16W ? 2 : 4)));
       f = end;
     }
   }
@@ -296,21 +304,21 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
 // preceding kernel started) with the routing lists built by the same launch from the
 // routing CTAs' slot map.
 int finalize_with_lists(const uint16_t* rows, const uint16_t* weights_bf16, int T, int K, int H, uint16_t* out,
-                        const uint32_t* smap, const uint8_t* rcount, int E, int32_t* offsets, int32_t* pairs,
+                        const uint32_t* smap, const uint8_t* below, int E, int32_t* offsets, int32_t* pairs,
                         cudaStream_t s) {
   if (T < 1 || K < 1 || K > MOE_MAX_TOPK || H < 8 || H % 8 != 0 || E < 1 || E > MOE_MAX_EXPERTS)
     return MOE_ERR_INVALID_ARGUMENT;
   if ((long long)T * K > (1LL << 31) - 1 || (long long)T * (H / 8) > (1LL << 31) * (long long)kThreads - 1)
     return MOE_ERR_CAPACITY;
-  if (!rows || !weights_bf16 || !out || !smap || !rcount || !offsets || !pairs) return MOE_ERR_INVALID_ARGUMENT;
-  if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(weights_bf16, 2) || !aligned(smap, 4) ||
+  if (!rows || !weights_bf16 || !out || !smap || !below || !offsets || !pairs) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(weights_bf16, 2) || !aligned(smap, 4) || !aligned(below, 16) ||
       !aligned(offsets, 4) || !aligned(pairs, 4))
     return MOE_ERR_ALIGNMENT;
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   FinArgs a{rows, (long long)T * K, nullptr, weights_bf16, nullptr, 1.0f, T, K, H, out, dev.error_word, 0};
-  a.lm = lists_impl::MapArgs{smap, rcount, T, K, E, offsets, pairs};
+  a.lm = lists_impl::MapArgs{smap, below, T, K, E, offsets, pairs};
   a.n_list = (E + lists_impl::kMaxEpc - 1) / lists_impl::kMaxEpc;
   if (K == 16) return launch_one<16, false, true, false, true>(a, dev.sm_count, s);
   if (K == 8) return launch_one<8, false, true, false, true>(a, dev.sm_count, s);

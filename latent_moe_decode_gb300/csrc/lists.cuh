@@ -219,17 +219,19 @@ __device__ __forceinline__ void lists_range_cta(const ListArgs& a, int range, Ra
 }
 
 // ---------------------------------------------------------------------------------
-// The one-call step's lists from the routing CTAs' slot map (TopkArgs::smap): the map
-// holds, for every 4-token block b and expert e, the four tokens' slots of e (0xFF when
-// absent), so expert e's list is the present bytes of column e in (b, byte) order --
-// token order -- and its pair codes are (4b + i) * K + slot. One CTA of W warps builds
-// the lists of one range of 32 experts (lane = expert): warp w takes a contiguous share
-// of the blocks; pass 1 counts each expert's pairs in the share, the shares' counts are
-// scanned per expert and the range's totals over the experts, the lower ranges' pair
-// counts (rcount) give the base, and pass 2 writes every pair in order. No atomics.
+// The one-call step's lists from the routing CTAs' slot map (TopkArgs::smap): for every
+// 4-token block b and expert e, the four tokens' slots of e (0xFF when absent), stored
+// range-major (smap[r][b][j], e = 32 r + j), so a range's map is contiguous and expert
+// e's list is the present bytes of its column in (b, byte) order -- token order --
+// with pair codes (4b + i) * K + slot. One CTA of W warps builds the lists of one range
+// of 32 experts (lane = expert): the pairs below the range are the sum of one row of
+// `below` (written by the routing CTAs); warp w takes a contiguous share of the blocks;
+// pass 1 counts each expert's pairs in the share, the shares' counts are scanned per
+// expert and the range's totals over the experts, and pass 2 writes every pair in
+// order. No atomics.
 struct MapArgs {
-  const uint32_t* smap;   // [nb][E]
-  const uint8_t* rcount;  // [nb][ceil(E / 32)]
+  const uint32_t* smap;  // [ceil(E / 32)][nb][32]
+  const uint8_t* below;  // [ceil(E / 32)][nbp]
   int T, K, E;
   int32_t* offsets;
   int32_t* pairs;
@@ -241,30 +243,36 @@ struct MapSmem {
   int base[W];
 };
 
-constexpr int kMapUnroll = 16;  // map words in flight per lane
+constexpr int kMapUnroll = 64;  // map words in flight per lane
 
 template <int W>
 __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapSmem<W>& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nb = (m.T + 3) / 4, nr = (m.E + 31) / 32;
+  const int nb = (m.T + 3) / 4, nbp = (nb + 15) / 16 * 16;
   const int e = range * kMaxEpc + lane;
   const bool ev = e < m.E;
-  // the pairs of the lower ranges
+  // the pairs below the range: one row of nbp bytes (16-byte pieces, zero past nb)
   int lower = 0;
-  for (int i = threadIdx.x; i < nb * range; i += W * 32) {
-    const int b = i / range;
-    lower += m.rcount[(size_t)b * nr + (i - b * range)];
+  const uint8_t* brow = m.below + (size_t)range * nbp;
+  for (int i = threadIdx.x * 16; i < nbp; i += W * 32 * 16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(brow + i);
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int by = 0; by < 4; ++by)
+        if (i + 4 * j + by < nb) lower += (q[j] >> (8 * by)) & 0xFFu;
   }
   lower = __reduce_add_sync(kFull, lower);
   if (lane == 0) sm.base[warp] = lower;
   const int per = (nb + W - 1) / W, b0 = min(nb, warp * per), b1 = min(nb, b0 + per);
-  const uint32_t* col = m.smap + e;
+  const uint32_t* col = m.smap + (size_t)range * nb * 32 + lane;
   // pass 1: expert e's pairs in this warp's blocks
   int c = 0;
   for (int b = b0; b < b1; b += kMapUnroll) {
     uint32_t wv[kMapUnroll];
 #pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) wv[u] = (ev && b + u < b1) ? __ldcg(col + (size_t)(b + u) * m.E) : 0xFFFFFFFFu;
+    for (int u = 0; u < kMapUnroll; ++u) wv[u] = b + u < b1 ? __ldcg(col + (size_t)(b + u) * 32) : 0xFFFFFFFFu;
 #pragma unroll
     for (int u = 0; u < kMapUnroll; ++u) c += __popc(~wv[u] & 0x80808080u);
   }
@@ -298,7 +306,7 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
   for (int b = b0; b < b1; b += kMapUnroll) {
     uint32_t wv[kMapUnroll];
 #pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) wv[u] = (ev && b + u < b1) ? __ldcg(col + (size_t)(b + u) * m.E) : 0xFFFFFFFFu;
+    for (int u = 0; u < kMapUnroll; ++u) wv[u] = b + u < b1 ? __ldcg(col + (size_t)(b + u) * 32) : 0xFFFFFFFFu;
 #pragma unroll
     for (int u = 0; u < kMapUnroll; ++u) {
 #pragma unroll

@@ -55,7 +55,7 @@ bool route_uses_warp_body(int E, const float* logits, const float* bias, const f
 int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
                    uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part, int S,
-                   uint32_t* smap, uint8_t* rcount) {
+                   uint32_t* smap, uint8_t* below) {
   using namespace moe::topk_impl;
   if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARGUMENT;
   if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK) return MOE_ERR_CAPACITY;
@@ -70,7 +70,7 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   const long long qblocks = (nchunks + per - 1) / per;
   // (with partials, the warp body also stores the logits as float4)
   const bool warp = route_uses_warp_body(E, logits, bias, part, S);
-  if (smap && (!warp || !rcount)) return MOE_ERR_INVALID_ARGUMENT;
+  if (smap && (!warp || !below || !aligned(below, 16))) return MOE_ERR_INVALID_ARGUMENT;
   const long long rblocks = route_blocks(T, warp);
   if (rblocks + qblocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
   DeviceInfo dev;
@@ -85,7 +85,7 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
     a.discard = (E % 32 == 0 && aligned(part, 128)) ? 1 : 0;
   }
   a.smap = smap;
-  a.rcount = rcount;
+  a.below = below;
   const dim3 grid((unsigned)(rblocks + qblocks)), block(kThreads);
   const int qb = (int)qblocks, rb = (int)rblocks, qw = latent_ready ? 0 : 1;
 #define MOE_RQ_LAUNCH(NJ, W)                                                                                      \

@@ -101,11 +101,12 @@ struct TopkArgs {
   float* logits_out = nullptr;
   int discard = 0;
   // Optional (warp body): each 4-token routing CTA b also writes, for the routing lists
-  // that the one-call step builds in its Finalize launch, smap[b][e] (byte i: the slot
-  // of expert e in token 4b + i, 0xFF when that token did not pick e) and
-  // rcount[b][r] (its pairs with an expert in range r of 32 experts).
+  // that the one-call step builds in its Finalize launch, the slot map (range-major:
+  // word smap[r][b][j] for expert e = 32 r + j; byte i: the slot of e in token 4b + i,
+  // 0xFF when that token did not pick e) and below[r][b] (its pairs with an expert
+  // below 32 r; rows of ceil(nb / 16) * 16 bytes, nb = ceil(T / 4)).
   uint32_t* smap = nullptr;
-  uint8_t* rcount = nullptr;
+  uint8_t* below = nullptr;
 };
 
 constexpr int kThreads = 128;  // both bodies: CTAs of 4 warps
@@ -629,8 +630,8 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
     __shared__ WarpScratch ws[kWarps];
     __shared__ uint32_t s_map[kWarpMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = blk * kWarps + warp;
-    if (a.smap)
-      for (int i = threadIdx.x; i < a.E; i += kThreads) s_map[i] = 0xFFFFFFFFu;
+    if (a.smap)  // (experts past E up to the range end stay absent)
+      for (int i = threadIdx.x; i < (a.E + 31) / 32 * 32; i += kThreads) s_map[i] = 0xFFFFFFFFu;
     if (t < a.T) topk_token_warp<NJ, PART>(a, t, ws[warp]);
     if (a.smap) {
       __syncthreads();  // the map is cleared and every token's slots are known
@@ -638,13 +639,22 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
       // distinct, so every byte has one writer)
       if (t < a.T && lane < a.K) reinterpret_cast<uint8_t*>(s_map)[4 * ws[warp].slot_id[lane] + warp] = (uint8_t)lane;
       __syncthreads();
-      const int nr = (a.E + 31) / 32;
-      for (int r = threadIdx.x; r < nr; r += kThreads) {
-        int c = 0;  // slot bytes are below 0x80, absent ones 0xFF
-        for (int e = 32 * r; e < min(a.E, 32 * r + 32); ++e) c += __popc(~s_map[e] & 0x80808080u);
-        a.rcount[(size_t)blk * nr + r] = (uint8_t)c;
+      const int nr = (a.E + 31) / 32, nb = (a.T + 3) / 4, nbp = (nb + 15) / 16 * 16;
+      if (warp == 0) {
+        // this block's pairs below each range (nr <= 32 here: E <= kWarpMaxE): a scan of
+        // the per-range counts (slot bytes are below 0x80, absent ones 0xFF)
+        int c = 0;
+        if (lane < nr)
+          for (int e = 32 * lane; e < 32 * lane + 32; ++e) c += __popc(~s_map[e] & 0x80808080u);
+        int inc = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(kFull, inc, d);
+          if (lane >= d) inc += y;
+        }
+        if (lane < nr) a.below[(size_t)lane * nbp + blk] = (uint8_t)(inc - c);
       }
-      for (int i = threadIdx.x; i < a.E; i += kThreads) a.smap[(size_t)blk * a.E + i] = s_map[i];
+      for (int i = threadIdx.x; i < nr * 32; i += kThreads) a.smap[((size_t)(i >> 5) * nb + blk) * 32 + (i & 31)] = s_map[i];
     }
   } else {
     topk_token_cta<NJ, PART>(a, blk);
