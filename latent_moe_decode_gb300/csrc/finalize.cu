@@ -67,6 +67,13 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr int kStages = 2;
 
+// The lists role of a LISTS launch, kept out of line: inlined, its code changed how the
+// compiler scheduled Finalize's loop (more registers), which cost the row stream 7 us
+// at T = 1020.
+__device__ __noinline__ void build_lists(const lists_impl::MapArgs& m, int range, uint4* smem) {
+  lists_impl::lists_from_map<kThreads / 32>(m, range, *reinterpret_cast<lists_impl::MapSmem<kThreads / 32>*>(smem));
+}
+
 // KT: compile-time K (0 = runtime K, up to MOE_MAX_TOPK). LISTS: the launch also builds
 // the routing lists (the one-call step): its first a.n_list CTAs do that, beside the
 // row stream, and the others run Finalize.
@@ -78,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     if (cta < a.n_list) {
       grid_launch_dependents();
       grid_wait();  // the slot map comes from the preceding kernel
-      lists_impl::lists_from_map<kThreads / 32>(a.lm, cta, *reinterpret_cast<lists_impl::MapSmem<kThreads / 32>*>(slots));
+      build_lists(a.lm, cta, slots);
       return;
     }
     cta -= a.n_list;

@@ -243,7 +243,7 @@ struct MapSmem {
   int base[W];
 };
 
-constexpr int kMapUnroll = 64;  // map words in flight per lane
+constexpr int kMapUnroll = 32;  // map words in flight per lane
 
 template <int W>
 __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapSmem<W>& sm) {
@@ -251,6 +251,15 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
   const int nb = (m.T + 3) / 4, nbp = (nb + 15) / 16 * 16;
   const int e = range * kMaxEpc + lane;
   const bool ev = e < m.E;
+  const int per = (nb + W - 1) / W, b0 = min(nb, warp * per), b1 = min(nb, b0 + per);
+  const uint32_t* col = m.smap + (size_t)range * nb * 32 + lane;
+  auto load = [&](int b, uint32_t (&wv)[kMapUnroll]) {
+#pragma unroll
+    for (int u = 0; u < kMapUnroll; ++u) wv[u] = b + u < b1 ? __ldcg(col + (size_t)(b + u) * 32) : 0xFFFFFFFFu;
+  };
+  // the first batch of this warp's words (kept for pass 2), issued before the below row
+  uint32_t first[kMapUnroll];
+  load(b0, first);
   // the pairs below the range: one row of nbp bytes (16-byte pieces, zero past nb)
   int lower = 0;
   const uint8_t* brow = m.below + (size_t)range * nbp;
@@ -263,19 +272,18 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
       for (int by = 0; by < 4; ++by)
         if (i + 4 * j + by < nb) lower += (q[j] >> (8 * by)) & 0xFFu;
   }
-  lower = __reduce_add_sync(kFull, lower);
-  if (lane == 0) sm.base[warp] = lower;
-  const int per = (nb + W - 1) / W, b0 = min(nb, warp * per), b1 = min(nb, b0 + per);
-  const uint32_t* col = m.smap + (size_t)range * nb * 32 + lane;
   // pass 1: expert e's pairs in this warp's blocks
   int c = 0;
-  for (int b = b0; b < b1; b += kMapUnroll) {
-    uint32_t wv[kMapUnroll];
 #pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) wv[u] = b + u < b1 ? __ldcg(col + (size_t)(b + u) * 32) : 0xFFFFFFFFu;
+  for (int u = 0; u < kMapUnroll; ++u) c += __popc(~first[u] & 0x80808080u);
+  for (int b = b0 + kMapUnroll; b < b1; b += kMapUnroll) {
+    uint32_t wv[kMapUnroll];
+    load(b, wv);
 #pragma unroll
     for (int u = 0; u < kMapUnroll; ++u) c += __popc(~wv[u] & 0x80808080u);
   }
+  lower = __reduce_add_sync(kFull, lower);
+  if (lane == 0) sm.base[warp] = lower;
   sm.cnt[warp][lane] = c;
   __syncthreads();
   if (warp == 0) {
@@ -303,10 +311,7 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
   __syncthreads();
   // pass 2: the pairs of expert e in this warp's blocks, in token order
   int pos = sm.cnt[warp][lane];
-  for (int b = b0; b < b1; b += kMapUnroll) {
-    uint32_t wv[kMapUnroll];
-#pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) wv[u] = b + u < b1 ? __ldcg(col + (size_t)(b + u) * 32) : 0xFFFFFFFFu;
+  auto place = [&](int b, const uint32_t (&wv)[kMapUnroll]) {
 #pragma unroll
     for (int u = 0; u < kMapUnroll; ++u) {
 #pragma unroll
@@ -315,6 +320,12 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
         if (slot != 0xFFu) m.pairs[pos++] = (4 * (b + u) + i) * m.K + (int)slot;
       }
     }
+  };
+  place(b0, first);
+  for (int b = b0 + kMapUnroll; b < b1; b += kMapUnroll) {
+    uint32_t wv[kMapUnroll];
+    load(b, wv);
+    place(b, wv);
   }
 }
 

@@ -618,6 +618,7 @@ __device__ __forceinline__ void topk_token_cta(const TopkArgs& a, const int t) {
 // partials) before reading.
 template <int NJ, bool WARP, bool PART>
 __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
+  __shared__ uint32_t s_map[WARP ? kWarpMaxE : 1];
   grid_launch_dependents();
   if (!PART && (a.E & 3) == 0) {
     // the logits rows' DRAM fetch overlaps the preceding kernel's end (a hint only)
@@ -625,13 +626,12 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
     if ((threadIdx.x & (WARP ? 31 : 127)) == 0 && t < a.T && aligned(a.logits, 16))
       prefetch_l2(a.logits + (size_t)t * a.E, (uint32_t)a.E * 4u);
   }
+  if (WARP && a.smap)  // cleared before the wait (experts past E up to the range end stay absent)
+    for (int i = threadIdx.x; i < (a.E + 31) / 32 * 32; i += kThreads) s_map[i] = 0xFFFFFFFFu;
   grid_wait();
   if constexpr (WARP) {
     __shared__ WarpScratch ws[kWarps];
-    __shared__ uint32_t s_map[kWarpMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = blk * kWarps + warp;
-    if (a.smap)  // (experts past E up to the range end stay absent)
-      for (int i = threadIdx.x; i < (a.E + 31) / 32 * 32; i += kThreads) s_map[i] = 0xFFFFFFFFu;
     if (t < a.T) topk_token_warp<NJ, PART>(a, t, ws[warp]);
     if (a.smap) {
       __syncthreads();  // the map is cleared and every token's slots are known
