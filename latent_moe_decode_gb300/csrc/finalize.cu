@@ -53,6 +53,7 @@ struct FinArgs {
   // routing CTAs' slot map (one 32-expert range each) instead of summing rows
   lists_impl::MapArgs lm;
   int n_list;
+  int map_chunk;  // blocks of the slot map a lists CTA stages at a time
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
@@ -70,8 +71,9 @@ constexpr int kStages = 2;
 // The lists role of a LISTS launch, kept out of line: inlined, its code changed how the
 // compiler scheduled Finalize's loop (more registers), which cost the row stream 7 us
 // at T = 1020.
-__device__ __noinline__ void build_lists(const lists_impl::MapArgs& m, int range, uint4* smem) {
-  lists_impl::lists_from_map<kThreads / 32>(m, range, *reinterpret_cast<lists_impl::MapSmem<kThreads / 32>*>(smem));
+__device__ __noinline__ void build_lists(const lists_impl::MapArgs& m, int range, uint4* smem, int chunk) {
+  lists_impl::lists_from_map<kThreads / 32>(m, range, *reinterpret_cast<lists_impl::MapSmem<kThreads / 32>*>(smem),
+                                            chunk);
 }
 
 // KT: compile-time K (0 = runtime K, up to MOE_MAX_TOPK). LISTS: the launch also builds
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     if (cta < a.n_list) {
       grid_launch_dependents();
       grid_wait();  // the slot map comes from the preceding kernel
-      build_lists(a.lm, cta, slots);
+      build_lists(a.lm, cta, slots, a.map_chunk);
       return;
     }
     cta -= a.n_list;
@@ -244,9 +246,16 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
 }
 
 template <int KT, bool G, bool B, bool S, bool LISTS = false>
-int launch_one(const FinArgs& a, int sm_count, cudaStream_t s) {
+int launch_one(FinArgs a, int sm_count, cudaStream_t s) {
   size_t smem = (size_t)kStages * ((KT ? KT : a.K) + (S ? 1 : 0)) * kThreads * 16;
-  if (LISTS && smem < sizeof(lists_impl::MapSmem<kThreads / 32>)) smem = sizeof(lists_impl::MapSmem<kThreads / 32>);
+  if (LISTS) {
+    // the lists CTAs stage their range's map in the shared memory Finalize's stages
+    // use: all of it when it fits (one round trip), else chunks of what fits
+    constexpr size_t head = lists_impl::map_smem_bytes<kThreads / 32>(0);
+    if (smem < head + 32 * 4) smem = head + 32 * 4;
+    const int nb = (a.T + 3) / 4;
+    a.map_chunk = (int)min((size_t)nb, (smem - head) / (32 * 4));
+  }
   auto kern = finalize_kernel<KT, G, B, S, LISTS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
   int per_sm = 0;

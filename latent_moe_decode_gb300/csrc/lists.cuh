@@ -241,26 +241,33 @@ template <int W>
 struct MapSmem {
   int cnt[W][kMaxEpc];  // per (warp, expert): pairs in the warp's share, then where they start
   int base[W];
+  __align__(16) uint32_t words[1];  // [chunk blocks][32]: the range's map, staged (bytes past the struct's end)
 };
 
-constexpr int kMapUnroll = 32;  // map words in flight per lane
-
+// Shared memory the lists role needs to stage `blocks` blocks of a range's map.
 template <int W>
-__device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapSmem<W>& sm) {
+__host__ __device__ constexpr size_t map_smem_bytes(int blocks) {
+  return sizeof(MapSmem<W>) + (size_t)blocks * 32 * 4;
+}
+
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+               "l"(src)
+               : "memory");
+}
+
+// chunk: the blocks of the range's map staged at a time (the CTA's shared memory holds
+// map_smem_bytes<W>(chunk)). All of a chunk's words (and the below row) are requested
+// at once -- a single round trip, however busy the memory system -- and the passes read
+// shared memory.
+template <int W>
+__device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapSmem<W>& sm, int chunk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nb = (m.T + 3) / 4, nbp = (nb + 15) / 16 * 16;
   const int e = range * kMaxEpc + lane;
   const bool ev = e < m.E;
-  const int per = (nb + W - 1) / W, b0 = min(nb, warp * per), b1 = min(nb, b0 + per);
-  const uint32_t* col = m.smap + (size_t)range * nb * 32 + lane;
-  auto load = [&](int b, uint32_t (&wv)[kMapUnroll]) {
-#pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) wv[u] = b + u < b1 ? __ldcg(col + (size_t)(b + u) * 32) : 0xFFFFFFFFu;
-  };
-  // the first batch of this warp's words (kept for pass 2), issued before the below row
-  uint32_t first[kMapUnroll];
-  load(b0, first);
-  // the pairs below the range: one row of nbp bytes (16-byte pieces, zero past nb)
+  const uint32_t* rmap = m.smap + (size_t)range * nb * 32;
+  // the pairs below the range: one row of nbp bytes (zero past nb)
   int lower = 0;
   const uint8_t* brow = m.below + (size_t)range * nbp;
   for (int i = threadIdx.x * 16; i < nbp; i += W * 32 * 16) {
@@ -272,60 +279,64 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
       for (int by = 0; by < 4; ++by)
         if (i + 4 * j + by < nb) lower += (q[j] >> (8 * by)) & 0xFFu;
   }
-  // pass 1: expert e's pairs in this warp's blocks
-  int c = 0;
-#pragma unroll
-  for (int u = 0; u < kMapUnroll; ++u) c += __popc(~first[u] & 0x80808080u);
-  for (int b = b0 + kMapUnroll; b < b1; b += kMapUnroll) {
-    uint32_t wv[kMapUnroll];
-    load(b, wv);
-#pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) c += __popc(~wv[u] & 0x80808080u);
-  }
   lower = __reduce_add_sync(kFull, lower);
   if (lane == 0) sm.base[warp] = lower;
-  sm.cnt[warp][lane] = c;
-  __syncthreads();
-  if (warp == 0) {
-    int base = 0, tot = 0;
+  int start = 0;  // expert e's pairs in the chunks already placed
+  bool first = true;
+  for (int c0 = 0; c0 < nb; c0 += chunk) {
+    const int c1 = min(nb, c0 + chunk);
+    __syncthreads();  // the previous chunk's words are no longer read
+    for (int i = threadIdx.x; i < (c1 - c0) * 32; i += W * 32) cp_async4(&sm.words[i], rmap + (size_t)c0 * 32 + i);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // pass 1: expert e's pairs in this warp's share of the chunk
+    const int per = (c1 - c0 + W - 1) / W, b0 = min(c1, c0 + warp * per), b1 = min(c1, b0 + per);
+    int c = 0;
+    for (int b = b0; b < b1; ++b) c += __popc(~sm.words[(b - c0) * 32 + lane] & 0x80808080u);
+    sm.cnt[warp][lane] = c;
+    __syncthreads();
+    if (warp == 0) {
+      int tot = 0;
+      int wstart[W];
 #pragma unroll
-    for (int w = 0; w < W; ++w) base += sm.base[w];
-    int wstart[W];
+      for (int w = 0; w < W; ++w) {
+        wstart[w] = tot;
+        tot += sm.cnt[w][lane];
+      }
+      if (first) {  // the offsets: the range's pairs below, then a scan over its experts' totals
+        int base = 0;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      wstart[w] = tot;
-      tot += sm.cnt[w][lane];
+        for (int w = 0; w < W; ++w) base += sm.base[w];
+        // (totals over the whole map: a second look at the chunks when there are several)
+        int all = tot;
+#pragma unroll 8
+        for (int d0 = c1; d0 < nb; ++d0) all += ev ? __popc(~__ldcg(rmap + (size_t)d0 * 32 + lane) & 0x80808080u) : 0;
+        int inc = all;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(kFull, inc, d);
+          if (lane >= d) inc += y;
+        }
+        start = base + inc - all;
+        if (ev) m.offsets[e] = start;
+        if (e == m.E - 1) m.offsets[m.E] = start + all;
+      }
+#pragma unroll
+      for (int w = 0; w < W; ++w) sm.cnt[w][lane] = start + wstart[w];
+      start += tot;
     }
-    int inc = tot;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(kFull, inc, d);
-      if (lane >= d) inc += y;
-    }
-    const int off = base + inc - tot;
-#pragma unroll
-    for (int w = 0; w < W; ++w) sm.cnt[w][lane] = off + wstart[w];
-    if (ev) m.offsets[e] = off;
-    if (e == m.E - 1) m.offsets[m.E] = off + tot;
-  }
-  __syncthreads();
-  // pass 2: the pairs of expert e in this warp's blocks, in token order
-  int pos = sm.cnt[warp][lane];
-  auto place = [&](int b, const uint32_t (&wv)[kMapUnroll]) {
-#pragma unroll
-    for (int u = 0; u < kMapUnroll; ++u) {
+    __syncthreads();
+    // pass 2: expert e's pairs in this warp's share of the chunk, in token order
+    int pos = sm.cnt[warp][lane];
+    for (int b = b0; b < b1; ++b) {
+      const uint32_t wv = sm.words[(b - c0) * 32 + lane];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t slot = (wv[u] >> (8 * i)) & 0xFFu;
-        if (slot != 0xFFu) m.pairs[pos++] = (4 * (b + u) + i) * m.K + (int)slot;
+        const uint32_t slot = (wv >> (8 * i)) & 0xFFu;
+        if (slot != 0xFFu) m.pairs[pos++] = (4 * b + i) * m.K + (int)slot;
       }
     }
-  };
-  place(b0, first);
-  for (int b = b0 + kMapUnroll; b < b1; b += kMapUnroll) {
-    uint32_t wv[kMapUnroll];
-    load(b, wv);
-    place(b, wv);
+    first = false;
   }
 }
 
