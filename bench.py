@@ -799,6 +799,39 @@ def run_ncu_front(args):
     torch.cuda.synchronize()
 
 
+def run_ncu_call(args):
+    """One public call at T (default 1020), untimed, warmup + steps times (for profiler
+    captures of a single kernel): router, topk, lists, mxfp8, mxfp8_tcgen05, finalize,
+    finalize_shared (the Finalize-with-shared-expert workload)."""
+    import torch
+
+    import latent_moe_decode_gb300 as m
+
+    dev = torch.device("cuda", 0)
+    m.load()
+    T = args.T or T_WIDE
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    name = args.ncu_call
+    if name == "finalize_shared":
+        d = synth.finalize_shared_inputs()
+        rows, w, sh = bf(d["rows"]), bf(d["weights"]), bf(d["shared"])
+        idx = torch.from_numpy(d["row_index"]).to(dev)
+        call = lambda: m.finalize(rows, w, d["T"], d["K"], row_index=idx, shared=sh, scale=d["scale"])
+    else:
+        step = Step(T, dev, graph=False)
+        step.run()
+        torch.cuda.synchronize()
+        calls = step.calls()
+        if name == "mxfp8_tcgen05":
+            call = lambda: m.mxfp8_quantize_rows_tcgen05(step.latent)
+        else:
+            call = calls[name]
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    assert m.device_error(clear=True) == 0
+
+
 # ---------------------------------------------------------------------------
 ORACLE_STEPS = ("router", "topk", "lists", "mxfp8", "finalize")
 REF_TOKENS = 16  # tokens per reference-arm step (a fixed slice of the wide batch)
@@ -927,7 +960,10 @@ def main():
     ap.add_argument("--ncu-norm", action="store_true", help="run Finalize with the RMSNorm epilogue untimed (profiling)")
     ap.add_argument("--units", default=None, help="comma-separated T list: time the unit windows of the routing lists")
     ap.add_argument("--ncu-units", action="store_true", help="run the unit windows untimed (for profiler captures)")
-    ap.add_argument("--T", type=int, default=0, help="with --ncu-step: token count (default 1020)")
+    ap.add_argument("--ncu-call", default=None, choices=["router", "topk", "lists", "mxfp8", "mxfp8_tcgen05", "finalize",
+                                                         "finalize_shared"],
+                    help="run one public call untimed (for profiler captures of one kernel)")
+    ap.add_argument("--T", type=int, default=0, help="with --ncu-step / --ncu-call: token count (default 1020)")
     ap.add_argument("--router-algo", type=int, default=0, help="with --ncu-step: router kernel family")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -937,6 +973,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.ncu_step:
         run_ncu_step(args)
+        return
+    if args.ncu_call:
+        run_ncu_call(args)
         return
     if args.ncu_front:
         run_ncu_front(args)
