@@ -54,6 +54,10 @@ struct FinArgs {
   lists_impl::MapArgs lm;
   int n_list;
   int map_chunk;  // blocks of the slot map a lists CTA stages at a time
+  // GATHER: each lane takes `group` consecutive 32-fragment runs of one token in turn
+  // (its row indices and weights then load once per group); 1 when the fragments of a
+  // token are not a multiple of 32 * group
+  int group;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
@@ -104,12 +108,13 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   // indices choose the rows to copy: with a gather, everything waits
   const bool early = !a.wait_all && !GATHER;
   if (!early && threadIdx.x < 32) {
-    // The CTA's first fragments (128 consecutive ones, at most two tokens): the row
+    // The CTA's first fragments (at most two tokens' worth): the row
     // spans (without a gather), the shared-row spans, and the tokens' indices and weights
     // are asked of L2 before the wait, so their DRAM fetch overlaps the preceding
     // kernel's end (hints only: nothing is read into registers or shared memory).
     const int lane = threadIdx.x;
-    const long long lo = (long long)cta * kThreads, hi = min(lo + kThreads, total);
+    const long long span = GATHER ? (long long)kThreads * a.group : kThreads;  // the CTA's first fragments
+    const long long lo = (long long)cta * span, hi = min(lo + span, total);
     for (long long f = lo; f < hi;) {
       const int t = (int)(f / frags);
       const long long end = min(hi, (long long)(t + 1) * frags);
@@ -134,21 +139,40 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
   // into wraw[st]; returns the mask of rows not skipped.
   using WRaw = typename std::conditional<BF16W, uint16_t, float>::type;
   WRaw wraw[kStages][KM];
+  // GATHER: the row indices and raw weights of the token last issued (a lane's next
+  // items are of the same token while its group lasts)
+  int ctok = -1;
+  int cidx[GATHER ? KM : 1];  // (a row index is an int32; -1 for a skipped or out-of-range one)
+  WRaw cw[GATHER ? KM : 1];
   auto issue = [&](int st, long long fi, bool weights) -> uint32_t {
     uint32_t m = 0;
     if (fi < total) {
       const int t = (int)(fi / frags);
       const int col = (int)(fi - (long long)t * frags) * 8;
+      if constexpr (GATHER) {
+        if (t != ctok) {
+          ctok = t;
+#pragma unroll
+          for (int k = 0; k < KM; ++k) {
+            if (KT || k < K) {
+              const size_t ix = (size_t)t * K + k;
+              int r = __ldg(a.row_index + ix);
+              if (r < -1 || (long long)r >= a.n_rows) {
+                set_error(a.err, MOE_DEVERR_ROW_INDEX);
+                r = -1;
+              }
+              cidx[k] = r;
+              cw[k] = __ldg(static_cast<const WRaw*>(a.weights) + ix);
+            }
+          }
+        }
+      }
 #pragma unroll
       for (int k = 0; k < KM; ++k) {
         if (KT || k < K) {
           const size_t ix = (size_t)t * K + k;
-          long long r = GATHER ? (long long)__ldg(a.row_index + ix) : (long long)ix;
-          if (GATHER && (r < -1 || r >= a.n_rows)) {
-            set_error(a.err, MOE_DEVERR_ROW_INDEX);
-            r = -1;
-          }
-          if (weights) wraw[st][k] = __ldg(static_cast<const WRaw*>(a.weights) + ix);
+          const long long r = GATHER ? cidx[GATHER ? k : 0] : (long long)ix;
+          if (weights) wraw[st][k] = GATHER ? cw[GATHER ? k : 0] : __ldg(static_cast<const WRaw*>(a.weights) + ix);
           if (r != -1) {
             m |= 1u << k;
             cp_async16(base + (uint32_t)st * stage_bytes + (uint32_t)(k * kThreads * 16), a.rows + (size_t)r * H + col,
@@ -182,64 +206,95 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const FinArgs a) {
     grid_wait();  // the weights may come from the preceding kernel
     load_weights(0, f0);
     load_weights(1, f0 + stride);
-  } else {
+  } else if constexpr (!GATHER) {
     mask[0] = issue(0, f0, true);
+  } else {  // the first item of the gather order below: run 0 of group 0
+    mask[0] = issue(0, ((long long)cta * (kThreads / 32) + (threadIdx.x >> 5)) * 32LL * a.group + (threadIdx.x & 31), true);
   }
+  // sum item fi (waiting for its stage s) and store its 8 outputs
+  auto consume = [&](int s, long long fi) {
+    const int t = (int)(fi / frags);
+    const int col = (int)(fi - (long long)t * frags) * 8;
+    // the weights, loaded at issue, times routed_scaling_factor
+    float w[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      float wk = 0.0f;
+      if (KT || k < K) {
+        if constexpr (BF16W) wk = bf16_to_f32(wraw[s][k]); else wk = wraw[s][k];
+        if (a.scale != 1.0f) wk = __fmul_rn(wk, a.scale);
+      }
+      w[k] = wk;
+    }
+    cp_async_wait<kStages - 1>();
+    // FP32 fma over k in order
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+    const uint4* sl = slots + (size_t)s * SL * kThreads + threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (!((mask[s] >> k) & 1u)) continue;
+      const uint4 v = sl[k * kThreads];
+      const uint32_t q4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = __fmaf_rn(w[k], bf16_lo(q4[q]), acc[2 * q]);
+        acc[2 * q + 1] = __fmaf_rn(w[k], bf16_hi(q4[q]), acc[2 * q + 1]);
+      }
+    }
+    if (SHARED) {
+      const uint4 sh = sl[K * kThreads];
+      const uint32_t q4[4] = {sh.x, sh.y, sh.z, sh.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(q4[q]));
+        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(q4[q]));
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    st16(a.out + (size_t)t * H + col, o);
+  };
   bool ahead = early;  // the item one ahead is already issued
-  for (long long f = f0; f < total; f += kStages * stride) {
+  if constexpr (!GATHER) {
+    for (long long f = f0; f < total; f += kStages * stride) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
-      const long long fi = f + s * stride;
-      constexpr int kAhead = kStages - 1;
-      const int sn = (s + kAhead) % kStages;
-      if (!ahead) mask[sn] = issue(sn, fi + kAhead * stride, true);
-      ahead = false;
-      if (fi >= total) break;
-      const int t = (int)(fi / frags);
-      const int col = (int)(fi - (long long)t * frags) * 8;
-      // the weights, loaded at issue, times routed_scaling_factor
-      float w[KM];
-#pragma unroll
-      for (int k = 0; k < KM; ++k) {
-        float wk = 0.0f;
-        if (KT || k < K) {
-          if constexpr (BF16W) wk = bf16_to_f32(wraw[s][k]); else wk = wraw[s][k];
-          if (a.scale != 1.0f) wk = __fmul_rn(wk, a.scale);
-        }
-        w[k] = wk;
+      for (int s = 0; s < kStages; ++s) {
+        const long long fi = f + s * stride;
+        constexpr int kAhead = kStages - 1;
+        const int sn = (s + kAhead) % kStages;
+        if (!ahead) mask[sn] = issue(sn, fi + kAhead * stride, true);
+        ahead = false;
+        if (fi >= total) break;
+        consume(s, fi);
       }
-      cp_async_wait<kAhead>();
-      // FP32 fma over k in order
-      float acc[8];
+    }
+  } else {
+    // item q of this lane: run (q mod group) of its warp's group number q / group, each
+    // group 32 * group consecutive fragments of one token (one warp: 512 contiguous bytes
+    // of every row per item)
+    const long long wg = (long long)cta * (kThreads / 32) + (threadIdx.x >> 5), wtot = (long long)ncta * (kThreads / 32);
+    const int lane = threadIdx.x & 31, R = a.group;
+    auto item = [&](long long q) { return (wg + (q / R) * wtot) * 32LL * R + lane + 32LL * (q % R); };
+    for (long long q = 0;; q += kStages) {
+      bool end = false;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-      const uint4* sl = slots + (size_t)s * SL * kThreads + threadIdx.x;
-#pragma unroll
-      for (int k = 0; k < KM; ++k) {
-        if (!((mask[s] >> k) & 1u)) continue;
-        const uint4 v = sl[k * kThreads];
-        const uint32_t q4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[2 * q] = __fmaf_rn(w[k], bf16_lo(q4[q]), acc[2 * q]);
-          acc[2 * q + 1] = __fmaf_rn(w[k], bf16_hi(q4[q]), acc[2 * q + 1]);
+      for (int s = 0; s < kStages; ++s) {
+        const long long fi = item(q + s);
+        constexpr int kAhead = kStages - 1;
+        const int sn = (s + kAhead) % kStages;
+        mask[sn] = issue(sn, item(q + s + kAhead), true);
+        if (fi >= total) {
+          end = true;
+          break;
         }
+        consume(s, fi);
       }
-      if (SHARED) {
-        const uint4 sh = sl[K * kThreads];
-        const uint32_t q4[4] = {sh.x, sh.y, sh.z, sh.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(q4[q]));
-          acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(q4[q]));
-        }
-      }
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      st16(a.out + (size_t)t * H + col, o);
+      if (end) break;
     }
   }
   cp_async_wait<0>();
@@ -311,6 +366,8 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
   FinArgs a{rows, (long long)n_rows, row_index, weights, shared, routed_scaling_factor, T, K, H, out, dev.error_word,
             rows_ready ? 0 : 1};
   const bool gather = row_index != nullptr, bf16w = weights_dtype == MOE_DTYPE_BF16, sh = shared != nullptr;
+  const int frags = H / 8;
+  a.group = frags % 128 == 0 ? 4 : (frags % 64 == 0 ? 2 : 1);
   if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, dev.sm_count, s);
   if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, dev.sm_count, s);
   return launch_variant<0>(a, gather, bf16w, sh, dev.sm_count, s);

@@ -284,6 +284,41 @@ __device__ __forceinline__ void load_logits4(const TopkArgs& a, int t, float4 (&
   }
 }
 
+// The warp body's rare path -- heavy ties, NaN or infinite keys (fewer than K or more
+// than 64 candidates, or no finite bound): exact keys of all experts (lane l: experts
+// l + 32 i, from the logits row staged in shared memory), then K rounds of a warp argmax
+// over (key descending, expert ascending). Out of line and not unrolled, so that its code
+// does not crowd the instruction cache of the common path.
+static __device__ __noinline__ void select_all_exact(const TopkArgs& a, const float* xrow, int32_t* slot_id, float* slot_s) {
+  const int lane = threadIdx.x & 31, E = a.E, n = (E + 31) / 32;
+  uint32_t key[kWarpMaxE / 32];
+  float sc[kWarpMaxE / 32];
+#pragma unroll 1
+  for (int i = 0; i < n; ++i) {
+    const int e = 32 * i + lane;
+    key[i] = e < E ? exact_key(a, xrow[e], a.bias ? __ldg(a.bias + e) : 0.f, &sc[i]) : 0u;
+  }
+#pragma unroll 1
+  for (int k = 0; k < a.K; ++k) {
+    uint32_t bk = 0;
+    int bi = -1;
+#pragma unroll 1
+    for (int i = 0; i < n; ++i)
+      if (key[i] > bk) {  // ascending expert order within the lane: the first maximum wins
+        bk = key[i];
+        bi = i;
+      }
+    const uint32_t wk = __reduce_max_sync(kFull, bk);
+    const int we = (int)__reduce_min_sync(kFull, (bk == wk && bi >= 0) ? (uint32_t)(32 * bi + lane) : 0x7FFFFFFFu);
+    const float wsv = __shfl_sync(kFull, bi >= 0 ? sc[bi] : 0.f, we & 31);  // expert e lives in lane e % 32
+    if (lane == 0) {
+      slot_id[k] = we;
+      slot_s[k] = wsv;
+    }
+    if ((we & 31) == lane) key[we >> 5] = 0u;
+  }
+}
+
 template <int NJ4, bool PART>
 __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, WarpScratch& ws) {
   static_assert(4 * NJ4 <= 32, "one flag bit per expert of a lane");
@@ -381,42 +416,7 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
       ws.slot_s[r1] = s1;
     }
   } else {
-    // heavy ties, NaN or infinite keys: exact keys of all experts, then K rounds of a
-    // warp argmax over (key descending, expert ascending)
-    uint32_t key[NJ];
-    float sc[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ4; ++j) {
-      const float xs[4] = {x4[j].x, x4[j].y, x4[j].z, x4[j].w}, bs[4] = {b4[j].x, b4[j].y, b4[j].z, b4[j].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t kx = exact_key(a, xs[i], bs[i], &sc[4 * j + i]);
-        key[4 * j + i] = 128 * j + 4 * lane < E ? kx : 0u;
-      }
-    }
-    for (int k = 0; k < K; ++k) {
-      uint32_t bk = 0;
-      int be = 0x7FFFFFFF;
-      float bs = 0.f;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        if (key[j] > bk) {  // ascending expert order within the lane: the first maximum wins
-          bk = key[j];
-          be = 128 * (j >> 2) + 4 * lane + (j & 3);
-          bs = sc[j];
-        }
-      }
-      const uint32_t wk = __reduce_max_sync(kFull, bk);
-      const int we = (int)__reduce_min_sync(kFull, bk == wk ? (uint32_t)be : 0x7FFFFFFFu);
-      const float wsv = __shfl_sync(kFull, bs, (we >> 2) & 31);  // expert e lives in lane (e / 4) % 32
-      if (lane == 0) {
-        ws.slot_id[k] = we;
-        ws.slot_s[k] = wsv;
-      }
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if (128 * (j >> 2) + 4 * lane + (j & 3) == we) key[j] = 0u;
-    }
+    select_all_exact(a, ws.x, ws.slot_id, ws.slot_s);
   }
   __syncwarp();
   // 5) weights
