@@ -3,9 +3,8 @@
 // router is launched the ordinary way (it starts once its predecessor has completed)
 // and signals its dependents after that; the later kernels use programmatic dependent
 // launch and execute griddepcontrol.wait before they read anything an earlier kernel
-// of the step wrote. Reads of the step's own inputs may come first: the MXFP8 CTAs
-// quantise the latent without waiting, and Finalize issues its first row copies before
-// its wait (and reads top-K's weights only after it).
+// of the step wrote. Reads of the step's own inputs may come first: Finalize issues its
+// first row copies before its wait (and reads top-K's weights only after it).
 //
 // Source: vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.wide, WideMoE.run
 // (router -> route -> Finalize on one stream) and ...moe.ep.layer, EpMoeLayer.__call__.
@@ -63,17 +62,19 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   float* part = reinterpret_cast<float*>(ws);
   st = launch_router_partials(x, w, logits, T, H, E, dev.sm_count, part, dev.error_word, as_cuda(stream), &S);
   if (st != MOE_OK) return st;
-  // the latent is an input of the step, complete before the router started: the
-  // quantisation CTAs run beside the router instead of after it. The routing CTAs also
-  // write a slot map from which the Finalize launch builds the routing lists in CTAs of
-  // its own, beside its row stream (Finalize does not read the lists); where the
-  // warp-per-token body does not apply, the lists kernel runs between the two.
+  // The routing CTAs come first in the grid and the quantisation CTAs after them (as in
+  // the public call): measured, quantisation CTAs dispatched first to run beside the
+  // router could only use the SMs it leaves idle and delayed the routing CTAs by 1.4 to
+  // 2.8 us a step. The routing CTAs also write a slot map from which the Finalize launch
+  // builds the routing lists in CTAs of its own, beside its row stream (Finalize does not
+  // read the lists); where the warp-per-token body does not apply, the lists kernel runs
+  // between the two.
   const float* pp = S > 1 ? part : nullptr;
   const bool map = route_uses_warp_body(E, logits, bias, pp, S);
   uint32_t* smap = reinterpret_cast<uint32_t*>(ws + rws);
   uint8_t* below = ws + rws + smap_bytes(T, E);
   st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
-                      true, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr);
+                      false, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr);
   if (st != MOE_OK) return st;
   // Finalize starts its row copies (a step input) before its wait and reads top-K's
   // weights after it.

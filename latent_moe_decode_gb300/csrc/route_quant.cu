@@ -6,13 +6,13 @@
 // GB300 design: the two jobs share nothing, so in one grid the quantisation CTAs
 // stream the latent through HBM on the SMs the routing CTAs leave free, instead of
 // running after them. The routing CTAs run the top-K selection (topk.cuh: four tokens
-// per CTA, one per warp, at E <= 1024) and Q CTAs each quantise a 16 KB span of the
-// latent (mxfp8.cuh), one bulk copy per CTA. Inside moe_route_finalize the latent is an
-// input of the whole step, so the quantisation CTAs need not wait for the router (the
-// router signals its dependents only after its own wait): they come first in the grid
-// and run on the SMs the router leaves idle. Both bodies are the ones the separate
-// calls use, so the results are identical to moe_topk_route followed by
-// mxfp8_quantize_rows.
+// per CTA, one per warp, at E <= 1024) and come first in the grid; Q CTAs each quantise
+// a 16 KB span of the latent (mxfp8.cuh), one bulk copy per CTA. (With latent_ready the
+// order is reversed and the quantisation CTAs skip the wait, to run beside a preceding
+// kernel; the one-call step measured that slower: beside its router only the SMs the
+// router leaves idle could take them, and they delayed the routing CTAs.) Both bodies are
+// the ones the separate calls use, so the results are identical to moe_topk_route
+// followed by mxfp8_quantize_rows.
 #include "mxfp8.cuh"
 #include "topk.cuh"
 

@@ -489,18 +489,28 @@ int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* d
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  // No programmatic dependent launch for the router itself: launched early, its CTAs
-  // (a whole SM's shared memory each) only contended with the preceding kernel for
-  // SMs; measured, a chain of steps ran about 4 us a step faster without it. (The
-  // kernels after the router still launch early: it signals them.)
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? (CLUSTER ? 2 * p.S : 2) : (CLUSTER ? p.S : 1);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch only for the cluster plans (narrow and medium token
+  // tiles), whose launch then starts as the preceding kernel's CTAs leave (measured: the
+  // step 1 us faster at T = 64 and 256). The wide tiles' partials plan (T = 1020 in the
+  // step) is launched the ordinary way: early, its CTAs (a whole SM's shared memory each)
+  // only contended with the preceding Finalize (measured slower).
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (CLUSTER || PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = PAIR ? (CLUSTER ? 2 * p.S : 2) : (CLUSTER ? p.S : 1);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (CLUSTER && !FRONT) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = (CLUSTER || PAIR) ? 1 : 0;
-  if (attr[0].val.clusterDim.x > 8 &&
+  cfg.numAttrs = na;
+  if ((CLUSTER || PAIR) && attr[0].val.clusterDim.x > 8 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return MOE_ERR_CUDA;
   const int discard = (reinterpret_cast<uintptr_t>(part) & 127u) == 0 ? 1 : 0;
