@@ -489,11 +489,13 @@ int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* d
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  // Programmatic dependent launch only for the cluster plans (narrow and medium token
-  // tiles), whose launch then starts as the preceding kernel's CTAs leave (measured: the
-  // step 1 us faster at T = 64 and 256). The wide tiles' partials plan (T = 1020 in the
-  // step) is launched the ordinary way: early, its CTAs (a whole SM's shared memory each)
-  // only contended with the preceding Finalize (measured slower).
+  // Programmatic dependent launch only for the cluster plans of token tiles up to 128
+  // (T <= 256), whose launch then starts as the preceding kernel's CTAs leave (measured:
+  // the step 1 us faster at T = 64 and 256; the call alone at T = 16 / 64 / 256 6.7 /
+  // 7.4 / 11.0 us instead of 9.9 / 10.1 / 14.2). The 256-token tiles (T = 1020: the public
+  // call's 5-CTA clusters, the step's partials plan) are launched the ordinary way: early,
+  // their CTAs (a whole SM's shared memory each) only contended with the preceding kernel
+  // (measured slower: the call alone 22.8 instead of 19 us).
   cudaLaunchAttribute attr[2];
   int na = 0;
   if (CLUSTER || PAIR) {
@@ -503,7 +505,7 @@ int launch_bn(const uint16_t* x, const uint16_t* w, const uint16_t* w2, float* d
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (CLUSTER && !FRONT) {
+  if (CLUSTER && !FRONT && BN <= 128) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
