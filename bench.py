@@ -138,7 +138,7 @@ class Step:
     chain > 1, one more graph holds `chain` consecutive steps (one per copy in turn), as
     a decode loop captures consecutive layers in one graph."""
 
-    def __init__(self, T, device, seed=0, skew=False, router_algo=0, graph=True, nsets=1, chain=1):
+    def __init__(self, T, device, seed=0, skew=False, router_algo=0, graph=True, nsets=1, chain=1, rest=0):
         import torch
 
         import latent_moe_decode_gb300 as m
@@ -181,6 +181,15 @@ class Step:
                     for _ in range(chain):
                         self.run_direct(0)
                 self.warm_graph = g
+            # a graph of `rest` consecutive steps (a timed count that is not a multiple of
+            # `chain`), continuing the rotation
+            self.rest_graph = None
+            if rest > 0:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(rest):
+                        self.run_direct(i)
+                self.rest_graph = g
 
     def run_direct(self, i=0):
         st = self.sets[i % self.nsets]
@@ -388,7 +397,7 @@ def run_ours(args, rank, world, local_rank):
     m.load()
     T = T_WIDE
     nsets = n_copies(chain_bytes(algorithmic_bytes(T)))
-    step = Step(T, dev, seed=rank, nsets=nsets, chain=STEPS_PER_GRAPH)
+    step = Step(T, dev, seed=rank, nsets=nsets, chain=STEPS_PER_GRAPH, rest=args.steps % STEPS_PER_GRAPH)
     rf = step.rf
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -412,10 +421,10 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         # (a) K whole steps back to back, rotating over input sets that together exceed
         #     L2 (every step reads its inputs cold): CUDA graphs of STEPS_PER_GRAPH
-        #     consecutive steps, then single-step graphs for the remainder
+        #     consecutive steps, then one graph of the remaining K mod STEPS_PER_GRAPH steps
         barrier()
         full, rest = divmod(args.steps, STEPS_PER_GRAPH)
-        fns = [step.chain_graph.replay] * full + [lambda i=i: step.run(i) for i in range(rest)]
+        fns = [step.chain_graph.replay] * full + ([step.rest_graph.replay] if rest else [])
         ms = time_back_to_back(fns, stream) * len(fns) / args.steps
         barrier()
         # (b) each call alone, K launches back to back over rotated input copies
@@ -519,8 +528,8 @@ def run_ours(args, rank, world, local_rank):
                          f"({nsets * chain_bytes(ab) / 1e6:.0f} MB in rotation > 129 MB L2), so each step reads them cold; "
                          f"each call alone likewise over {copies} copies",
                    "launch": f"CUDA graphs of {STEPS_PER_GRAPH} consecutive steps (as a decode loop captures "
-                             "consecutive layers), replayed back to back; programmatic dependent launch between "
-                             "the kernels of a step",
+                             "consecutive layers; the steps past a multiple of 12 in one more graph), replayed back "
+                             "to back; programmatic dependent launch between the kernels of a step",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "chain_GB/s": round(chain_bytes(ab) / (ms * 1e-3) / 1e9, 1),
         "ms_per_step_flushed": round(flushed_ms, 5),
