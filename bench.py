@@ -363,7 +363,8 @@ def time_finalize_shared(dev, steps, warmup):
     return {"workload": "Finalize with shared expert: T=512, K=8, H=7168, routed rows [4096,7168] gathered by "
                         "permuted indices with 5 % -1, BF16 weights, routed_scaling_factor 2.5, shared rows [512,7168]",
             "us": round(ms * 1e3, 2), "alg_bytes": by, "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
-            "timing": f"{steps} launches back to back over {n} input copies (cold inputs every launch)"}
+            "timing": f"{steps} launches back to back over {n} input copies (cold inputs every launch)",
+            "traffic": kernel_traffic("finalize_shared")}
 
 
 def percentiles(v):
