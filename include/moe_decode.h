@@ -393,8 +393,10 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  * routing CTAs (four tokens each) also write each token's slots by expert to the
  * workspace; and Finalize, whose launch also builds the routing lists from those slots
  * in CTAs of its own (Finalize does not read the lists, so they are built beside its row
- * stream). Where top-K runs one CTA per token (E > 1024 or E % 4 != 0) the lists kernel
- * runs between the last two launches instead. For token tiles wider
+ * stream). Where top-K runs one CTA per token (E > 1024 or E % 4 != 0), or a range's
+ * slot map with its per-chunk counts does not fit the Finalize CTAs' shared memory in
+ * chunks (T above 65280 at K = 16, above 16256 at K = 8), the lists kernel runs between
+ * the last two launches instead. For token tiles wider
  * than 64 the router stores its split-K partials in the workspace instead of reducing
  * them, and the top-K launch sums each token's partials in the same split order before
  * selecting: the same logits, one on-chip exchange fewer. Arguments, layouts and

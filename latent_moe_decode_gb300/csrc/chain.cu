@@ -68,13 +68,17 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   // 2.8 us a step. The routing CTAs also write a slot map from which the Finalize launch
   // builds the routing lists in CTAs of its own, beside its row stream (Finalize does not
   // read the lists); where the warp-per-token body does not apply, the lists kernel runs
-  // between the two.
+  // between the two. Every CTA of this launch lets Finalize launch only when it is done:
+  // Finalize's persistent CTAs dispatched beside still-running CTAs of this launch found
+  // some SMs short of room, and the few that did not fit started only when another
+  // Finalize CTA ended, a full share late (measured: 2.2 us a step at T = 1020, 5 at
+  // T = 4096).
   const float* pp = S > 1 ? part : nullptr;
-  const bool map = route_uses_warp_body(E, logits, bias, pp, S);
+  const bool map = route_uses_warp_body(E, logits, bias, pp, S) && finalize_lists_fit(T, K);
   uint32_t* smap = reinterpret_cast<uint32_t*>(ws + rws);
   uint8_t* below = ws + rws + smap_bytes(T, E);
   st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
-                      false, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr);
+                      false, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr, true);
   if (st != MOE_OK) return st;
   // Finalize starts its row copies (a step input) before its wait and reads top-K's
   // weights after it.

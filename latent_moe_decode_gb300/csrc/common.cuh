@@ -36,7 +36,7 @@ int prefer_max_shared(const void* func);
 int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
                    uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part = nullptr,
-                   int S = 0, uint32_t* smap = nullptr, uint8_t* below = nullptr);
+                   int S = 0, uint32_t* smap = nullptr, uint8_t* below = nullptr, bool late_trigger = false);
 
 // Finalize (moe_finalize). With rows_ready (no row_index) the first row copies are
 // issued before the kernel waits for its predecessor, and everything else (weights) is
@@ -50,6 +50,7 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
 // before the preceding kernel started) whose launch also builds the routing lists, in
 // CTAs of its own beside the row stream, from the slot map the routing CTAs wrote
 // (route_quantize with smap).
+bool finalize_lists_fit(int T, int K);
 int finalize_with_lists(const uint16_t* rows, const uint16_t* weights_bf16, int T, int K, int H, uint16_t* out,
                         const uint32_t* smap, const uint8_t* below, int E, int32_t* offsets, int32_t* pairs,
                         cudaStream_t s);

@@ -306,10 +306,8 @@ int launch_one(FinArgs a, int sm_count, cudaStream_t s) {
   if (LISTS) {
     // the lists CTAs stage their range's map in the shared memory Finalize's stages
     // use: all of it when it fits (one round trip), else chunks of what fits
-    constexpr size_t head = lists_impl::map_smem_bytes<kThreads / 32>(0);
-    if (smem < head + 32 * 4) smem = head + 32 * 4;
-    const int nb = (a.T + 3) / 4;
-    a.map_chunk = (int)min((size_t)nb, (smem - head) / (32 * 4));
+    a.map_chunk = lists_impl::map_chunk_for<kThreads / 32>((a.T + 3) / 4, smem);
+    if (a.map_chunk < 1) return MOE_ERR_CAPACITY;
   }
   auto kern = finalize_kernel<KT, G, B, S, LISTS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
@@ -371,6 +369,15 @@ int finalize(const uint16_t* rows, int64_t n_rows, const int32_t* row_index, con
   if (K == 16) return launch_variant<16>(a, gather, bf16w, sh, dev.sm_count, s);
   if (K == 8) return launch_variant<8>(a, gather, bf16w, sh, dev.sm_count, s);
   return launch_variant<0>(a, gather, bf16w, sh, dev.sm_count, s);
+}
+
+// Whether the lists CTAs of finalize_with_lists have room for a range's map in chunks
+// (with their per-chunk counts) in the shared memory of Finalize's stages: T up to
+// 65280 at K = 16, 16256 at K = 8.
+bool finalize_lists_fit(int T, int K) {
+  if (T < 1 || K < 1 || K > MOE_MAX_TOPK) return false;
+  const size_t smem = (size_t)kStages * K * kThreads * 16;
+  return lists_impl::map_chunk_for<kThreads / 32>((T + 3) / 4, smem) >= 1;
 }
 
 // Finalize of the one-call step (rows t*K + k, BF16 weights; rows ready before the

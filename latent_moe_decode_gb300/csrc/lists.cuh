@@ -239,34 +239,65 @@ struct MapArgs {
 
 template <int W>
 struct MapSmem {
-  int cnt[W][kMaxEpc];  // per (warp, expert): pairs in the warp's share, then where they start
   int base[W];
-  __align__(16) uint32_t words[1];  // [chunk blocks][32]: the range's map, staged (bytes past the struct's end)
+  __align__(16) uint32_t words[1];  // [chunk blocks][32]: the range's map, staged; then the
+                                    // per-(chunk, warp, expert) counts (bytes past the struct's end)
 };
 
-// Shared memory the lists role needs to stage `blocks` blocks of a range's map.
+// Chunks of `chunk` blocks that cover a range's map of nb blocks.
+__host__ __device__ constexpr int map_chunks(int nb, int chunk) { return (nb + chunk - 1) / chunk; }
+
+// Shared memory the lists role needs to stage `chunk` blocks of a range's map of nb
+// blocks at a time, with its per-(chunk, warp, expert) counts.
 template <int W>
-__host__ __device__ constexpr size_t map_smem_bytes(int blocks) {
-  return sizeof(MapSmem<W>) + (size_t)blocks * 32 * 4;
+__host__ __device__ constexpr size_t map_smem_bytes(int nb, int chunk) {
+  return sizeof(MapSmem<W>) + (size_t)chunk * 32 * 4 + (size_t)map_chunks(nb, chunk) * W * 32 * 4;
 }
 
-__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+// The largest chunk (blocks) whose map_smem_bytes fits in `bytes`, or 0.
+template <int W>
+inline int map_chunk_for(int nb, size_t bytes) {
+  for (int chunk = nb; chunk >= 1;) {
+    if (map_smem_bytes<W>(nb, chunk) <= bytes) return chunk;
+    const size_t fixed = sizeof(MapSmem<W>) + (size_t)map_chunks(nb, chunk) * W * 32 * 4;
+    if (fixed >= bytes) return 0;
+    const int fit = (int)((bytes - fixed) / (32 * 4));
+    chunk = fit < chunk ? fit : chunk - 1;
+  }
+  return 0;
+}
+
+__device__ __forceinline__ void cp_async16_ca(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
                "l"(src)
                : "memory");
 }
 
+// Stage blocks [c0, c1) of the range's map: every 16-byte copy requested at once (one
+// round trip however busy the memory system is), then awaited.
+template <int W>
+__device__ __forceinline__ void stage_map(const uint32_t* rmap, int c0, int c1, uint32_t* words) {
+  __syncthreads();  // the previous chunk's words are no longer read
+  const uint4* src = reinterpret_cast<const uint4*>(rmap + (size_t)c0 * 32);
+  uint4* dst = reinterpret_cast<uint4*>(words);
+  for (int i = threadIdx.x; i < (c1 - c0) * 8; i += W * 32) cp_async16_ca(dst + i, src + i);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+}
+
 // chunk: the blocks of the range's map staged at a time (the CTA's shared memory holds
-// map_smem_bytes<W>(chunk)). All of a chunk's words (and the below row) are requested
-// at once -- a single round trip, however busy the memory system -- and the passes read
-// shared memory.
+// map_smem_bytes<W>(nb, chunk)). Pass 1 stages every chunk in turn and counts, per
+// (chunk, warp, expert), the pairs of the warp's share of the chunk; warp 0 then turns
+// the counts into the offsets and every (chunk, warp)'s start in each list; pass 2
+// places the pairs chunk by chunk, the chunk still staged first (with one chunk -- T up
+// to about 2000 at 16 KB of stages per warp -- the map is read once).
 template <int W>
 __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapSmem<W>& sm, int chunk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nb = (m.T + 3) / 4, nbp = (nb + 15) / 16 * 16;
+  const int nb = (m.T + 3) / 4, nbp = (nb + 15) / 16 * 16, nch = map_chunks(nb, chunk);
   const int e = range * kMaxEpc + lane;
-  const bool ev = e < m.E;
   const uint32_t* rmap = m.smap + (size_t)range * nb * 32;
+  int* ccnt = reinterpret_cast<int*>(sm.words + (size_t)chunk * 32);  // [nch][W][32]
   // the pairs below the range: one row of nbp bytes (zero past nb)
   int lower = 0;
   const uint8_t* brow = m.below + (size_t)range * nbp;
@@ -281,53 +312,45 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
   }
   lower = __reduce_add_sync(kFull, lower);
   if (lane == 0) sm.base[warp] = lower;
-  int start = 0;  // expert e's pairs in the chunks already placed
-  bool first = true;
-  for (int c0 = 0; c0 < nb; c0 += chunk) {
-    const int c1 = min(nb, c0 + chunk);
-    __syncthreads();  // the previous chunk's words are no longer read
-    for (int i = threadIdx.x; i < (c1 - c0) * 32; i += W * 32) cp_async4(&sm.words[i], rmap + (size_t)c0 * 32 + i);
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-    // pass 1: expert e's pairs in this warp's share of the chunk
+  // pass 1: expert e's pairs in this warp's share of each chunk
+  for (int ci = 0; ci < nch; ++ci) {
+    const int c0 = ci * chunk, c1 = min(nb, c0 + chunk);
+    stage_map<W>(rmap, c0, c1, sm.words);
     const int per = (c1 - c0 + W - 1) / W, b0 = min(c1, c0 + warp * per), b1 = min(c1, b0 + per);
     int c = 0;
     for (int b = b0; b < b1; ++b) c += __popc(~sm.words[(b - c0) * 32 + lane] & 0x80808080u);
-    sm.cnt[warp][lane] = c;
-    __syncthreads();
-    if (warp == 0) {
-      int tot = 0;
-      int wstart[W];
+    ccnt[(ci * W + warp) * 32 + lane] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int tot = 0, base = 0;
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
-        wstart[w] = tot;
-        tot += sm.cnt[w][lane];
-      }
-      if (first) {  // the offsets: the range's pairs below, then a scan over its experts' totals
-        int base = 0;
+    for (int w = 0; w < W; ++w) base += sm.base[w];
+    for (int i = 0; i < nch * W; ++i) tot += ccnt[i * 32 + lane];
+    int inc = tot;
 #pragma unroll
-        for (int w = 0; w < W; ++w) base += sm.base[w];
-        // (totals over the whole map: a second look at the chunks when there are several)
-        int all = tot;
-#pragma unroll 8
-        for (int d0 = c1; d0 < nb; ++d0) all += ev ? __popc(~__ldcg(rmap + (size_t)d0 * 32 + lane) & 0x80808080u) : 0;
-        int inc = all;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const int y = __shfl_up_sync(kFull, inc, d);
-          if (lane >= d) inc += y;
-        }
-        start = base + inc - all;
-        if (ev) m.offsets[e] = start;
-        if (e == m.E - 1) m.offsets[m.E] = start + all;
-      }
-#pragma unroll
-      for (int w = 0; w < W; ++w) sm.cnt[w][lane] = start + wstart[w];
-      start += tot;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, d);
+      if (lane >= d) inc += y;
     }
-    __syncthreads();
-    // pass 2: expert e's pairs in this warp's share of the chunk, in token order
-    int pos = sm.cnt[warp][lane];
+    int run = base + inc - tot;  // offsets[e]
+    if (e < m.E) m.offsets[e] = run;
+    if (e == m.E - 1) m.offsets[m.E] = run + tot;
+    for (int i = 0; i < nch * W; ++i) {  // (chunk, warp) order = token order
+      const int v = ccnt[i * 32 + lane];
+      ccnt[i * 32 + lane] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // pass 2: expert e's pairs in this warp's share of each chunk, in token order (the
+  // starts are known, so the chunk still staged goes first)
+  for (int k = 0; k < nch; ++k) {
+    const int ci = nch - 1 - k;
+    const int c0 = ci * chunk, c1 = min(nb, c0 + chunk);
+    if (k > 0) stage_map<W>(rmap, c0, c1, sm.words);
+    const int per = (c1 - c0 + W - 1) / W, b0 = min(c1, c0 + warp * per), b1 = min(c1, b0 + per);
+    int pos = ccnt[(ci * W + warp) * 32 + lane];
     for (int b = b0; b < b1; ++b) {
       const uint32_t wv = sm.words[(b - c0) * 32 + lane];
 #pragma unroll
@@ -336,7 +359,6 @@ __device__ __forceinline__ void lists_from_map(const MapArgs& m, int range, MapS
         if (slot != 0xFFu) m.pairs[pos++] = (4 * b + i) * m.K + (int)slot;
       }
     }
-    first = false;
   }
 }
 

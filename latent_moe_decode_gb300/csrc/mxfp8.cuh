@@ -27,11 +27,12 @@ __device__ __forceinline__ size_t tcgen05_scale_offset(int r, int c, int ct) {
 // input was complete before that kernel started). CEIL: the round-up scale rule (the
 // smallest power of two X with amax / X <= 448) instead of the OCP floor rule. TILED:
 // scales in the tcgen05 tile layout (nsc scale columns per row, ct column tiles)
-// instead of row-major.
+// instead of row-major. trigger: let the dependent grid launch at the start (else the
+// caller does, later).
 template <int THREADS, int UNROLL, bool CEIL = false, bool TILED = false>
 __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long long nchunks, uint8_t* __restrict__ q,
                                             uint8_t* __restrict__ scales, uint32_t* err, long long block,
-                                            bool wait = true, int nsc = 0, int ct = 0) {
+                                            bool wait = true, int nsc = 0, int ct = 0, bool trigger = true) {
   constexpr int kThreads = THREADS, kUnroll = UNROLL;
   __shared__ __align__(128) uint4 stage[kThreads * kUnroll];
   __shared__ __align__(8) uint64_t bar_mem;
@@ -44,7 +45,7 @@ __device__ __forceinline__ void mxfp8_block(const uint16_t* __restrict__ x, long
     mbar_fence_init();
   }
   __syncthreads();  // the barrier is initialised before any thread waits on it
-  grid_launch_dependents();
+  if (trigger) grid_launch_dependents();
   if (wait) {
     // the span's DRAM fetch overlaps the preceding kernel's end (a hint only)
     if (threadIdx.x == 0) prefetch_l2(x + cta0 * 8, (uint32_t)nch * 16u);

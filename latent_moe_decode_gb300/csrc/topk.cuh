@@ -615,11 +615,12 @@ __device__ __forceinline__ void topk_token_cta(const TopkArgs& a, const int t) {
 // The routing part of a launch: CTA `blk` of the routing CTAs. Warp body (NJ = experts
 // per lane / 4): its 4 warps take tokens 4 blk .. 4 blk + 3; CTA body (NJ = experts
 // per thread): token blk. Waits for the preceding kernel (which writes the logits or
-// partials) before reading.
+// partials) before reading. trigger: let the dependent grid launch at the start (else
+// the caller does, later).
 template <int NJ, bool WARP, bool PART>
-__device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
+__device__ __forceinline__ void route_block(const TopkArgs& a, int blk, bool trigger = true) {
   __shared__ uint32_t s_map[WARP ? kWarpMaxE : 1];
-  grid_launch_dependents();
+  if (trigger) grid_launch_dependents();
   if (!PART && (a.E & 3) == 0) {
     // the logits rows' DRAM fetch overlaps the preceding kernel's end (a hint only)
     const int t = WARP ? blk * kWarps + (int)(threadIdx.x >> 5) : blk;

@@ -100,12 +100,15 @@ def test_one_call_equals_four_calls(moe, T):
 @pytest.mark.parametrize("T,H,L,E,K", [(37, 512, 256, 100, 8), (300, 1024, 512, 1000, 16), (9, 256, 64, 40, 3),
                                        (130, 768, 128, 2048, 16),
                                        # the lists CTAs stage the slot map in chunks (more blocks than fit)
-                                       (1100, 512, 256, 100, 8), (400, 256, 64, 40, 3)])
+                                       (1100, 512, 256, 100, 8), (400, 256, 64, 40, 3),
+                                       # more chunks than their counts leave room for: the lists kernel
+                                       (16300, 128, 64, 96, 8)])
 def test_one_call_other_shapes(moe, orc, T, H, L, E, K):
     """The one-call step at shapes other than the decode layer's -- a last expert range
     of the lists shorter than 32 experts, K of 8, 3 and 16, E up to 2048 (the CTA-per-
-    token top-K and the separate lists kernel), slot maps staged in several chunks --
-    equals the four calls bit for bit, and its lists the oracle's."""
+    token top-K and the separate lists kernel), slot maps staged in several chunks, a
+    batch too large for the lists CTAs (the separate lists kernel) -- equals the four
+    calls bit for bit, and its lists the oracle's."""
     x = synth.normal_bf16(50 + T, 1, (T, H))
     w = synth.normal_bf16(50 + E, 2, (E, H), 0.02)
     bias = synth.normal_f32(50 + E, 3, (E,), 0.01)
