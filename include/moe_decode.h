@@ -389,9 +389,11 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  * i.e. Finalize combines the expanded expert rows (row t*K + k = token t's k-th
  * expert) with the BF16 routing weights, as the wide page's Finalize does. Every
  * output equals the four calls' bit for bit. It takes three launches (programmatic
- * dependent launch between them): the router; top-K with the MXFP8 of the latent, whose
- * routing CTAs (four tokens each) also write each token's slots by expert to the
- * workspace; and Finalize, whose launch also builds the routing lists from those slots
+ * dependent launch between them): the router, whose warps that wait for its tensor-core
+ * mainloop meanwhile quantise the latent to MXFP8 (for up to 8 tokens, whose router runs
+ * on the CUDA cores, the next launch does); top-K, whose routing CTAs (four tokens each)
+ * also write each token's slots by expert to the workspace; and Finalize, whose launch
+ * also builds the routing lists from those slots
  * in CTAs of its own (Finalize does not read the lists, so they are built beside its row
  * stream). Where top-K runs one CTA per token (E > 1024 or E % 4 != 0), or a range's
  * slot map with its per-chunk counts does not fit the Finalize CTAs' shared memory in

@@ -1,7 +1,6 @@
 // The routing-and-combine step as one call: three launches on the caller's stream --
-// the router; top-K with the MXFP8 of the latent; Finalize with the routing lists. The
-// router is launched the ordinary way (it starts once its predecessor has completed)
-// and signals its dependents after that; the later kernels use programmatic dependent
+// the router, whose epilogue warps quantise the latent to MXFP8 while its mainloop runs;
+// top-K; Finalize with the routing lists. The later kernels use programmatic dependent
 // launch and execute griddepcontrol.wait before they read anything an earlier kernel
 // of the step wrote. Reads of the step's own inputs may come first: Finalize issues its
 // first row copies before its wait (and reads top-K's weights only after it).
@@ -47,6 +46,10 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(logits, 4)) return MOE_ERR_ALIGNMENT;
   if (!aligned(rows, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(offsets, 4) || !aligned(pairs, 4))
     return MOE_ERR_ALIGNMENT;
+  if (L < 32 || L % 32 != 0 || !latent || !q || !scales) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(latent, 16) || !aligned(q, 8) || !aligned(scales, 8) || (weights && !aligned(weights, 4)) ||
+      !aligned(weights_bf16, 2) || (bias && !aligned(bias, 4)))
+    return MOE_ERR_ALIGNMENT;
   const size_t rws = router_part_bytes(T, H, E), mws = map_bytes(T, E);
   const size_t lws = moe_build_routing_lists_workspace(T, K, E);
   if (workspace_bytes < rws + mws + lws || !workspace) return MOE_ERR_WORKSPACE;
@@ -58,9 +61,18 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   // The router stores its split-K partials and the top-K launch sums them (in split
   // order, as the router's own reduction would: the same logits, bit for bit), so the
   // router skips its on-chip exchange; with one split it writes the logits itself.
+  // The router's epilogue warps, idle while its mainloop runs, also quantise the latent
+  // (a step input) to MXFP8; the few-token GEMV router leaves that to the top-K launch.
   int S = 1;
+  bool quantised = false;
   float* part = reinterpret_cast<float*>(ws);
-  st = launch_router_partials(x, w, logits, T, H, E, dev.sm_count, part, dev.error_word, as_cuda(stream), &S);
+  LatentQuant lq;
+  lq.x = latent;
+  lq.nchunks = (long long)T * (L / 8);
+  lq.q = q;
+  lq.scales = scales;
+  st = launch_router_partials(x, w, logits, T, H, E, dev.sm_count, part, dev.error_word, as_cuda(stream), &S, &lq,
+                              &quantised);
   if (st != MOE_OK) return st;
   // The routing CTAs come first in the grid and the quantisation CTAs after them (as in
   // the public call): measured, quantisation CTAs dispatched first to run beside the
@@ -68,17 +80,13 @@ extern "C" int moe_route_finalize(const uint16_t* x, const uint16_t* w, const fl
   // 2.8 us a step. The routing CTAs also write a slot map from which the Finalize launch
   // builds the routing lists in CTAs of its own, beside its row stream (Finalize does not
   // read the lists); where the warp-per-token body does not apply, the lists kernel runs
-  // between the two. Every CTA of this launch lets Finalize launch only when it is done:
-  // Finalize's persistent CTAs dispatched beside still-running CTAs of this launch found
-  // some SMs short of room, and the few that did not fit started only when another
-  // Finalize CTA ended, a full share late (measured: 2.2 us a step at T = 1020, 5 at
-  // T = 4096).
+  // between the two.
   const float* pp = S > 1 ? part : nullptr;
   const bool map = route_uses_warp_body(E, logits, bias, pp, S) && finalize_lists_fit(T, K);
   uint32_t* smap = reinterpret_cast<uint32_t*>(ws + rws);
   uint8_t* below = ws + rws + smap_bytes(T, E);
-  st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, T, L, q, scales,
-                      false, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr, true);
+  st = route_quantize(logits, bias, T, E, K, renormalize, scale, ids, weights, weights_bf16, latent, quantised ? 0 : T, L, q, scales,
+                      false, as_cuda(stream), pp, S, map ? smap : nullptr, map ? below : nullptr);
   if (st != MOE_OK) return st;
   // Finalize starts its row copies (a step input) before its wait and reads top-K's
   // weights after it.

@@ -36,7 +36,7 @@ int prefer_max_shared(const void* func);
 int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
                    uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part = nullptr,
-                   int S = 0, uint32_t* smap = nullptr, uint8_t* below = nullptr, bool late_trigger = false);
+                   int S = 0, uint32_t* smap = nullptr, uint8_t* below = nullptr);
 
 // Finalize (moe_finalize). With rows_ready (no row_index) the first row copies are
 // issued before the kernel waits for its predecessor, and everything else (weights) is

@@ -26,23 +26,18 @@ template <int NJ, bool WARP, bool PART>
 __global__ void __launch_bounds__(kThreads) route_quant_kernel(const TopkArgs a, const uint16_t* __restrict__ x,
                                                                long long nchunks, uint8_t* __restrict__ q,
                                                                uint8_t* __restrict__ scales, uint32_t* err, int qblocks,
-                                                               int rblocks, int quant_wait, int late) {
+                                                               int rblocks, int quant_wait) {
   // Blocks are dispatched in index order. When the quantisation CTAs need not wait they
   // come first and take the SMs that are free while the preceding kernel still runs;
-  // otherwise the routing CTAs (the longer ones) come first. late: every CTA lets the
-  // dependent grid launch only when it is done (else at its start).
+  // otherwise the routing CTAs (the longer ones) come first.
   const int b = (int)blockIdx.x;
   if (quant_wait) {
-    if (b < rblocks) route_block<NJ, WARP, PART>(a, b, !late);
-    else
-      mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)(b - rblocks), true, 0, 0,
-                                                      !late);
+    if (b < rblocks) route_block<NJ, WARP, PART>(a, b);
+    else mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)(b - rblocks), true);
   } else {
-    if (b < qblocks)
-      mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)b, false, 0, 0, !late);
-    else route_block<NJ, WARP, PART>(a, b - qblocks, !late);
+    if (b < qblocks) mxfp8_impl::mxfp8_block<kThreads, kQuantUnroll>(x, nchunks, q, scales, err, (long long)b, false);
+    else route_block<NJ, WARP, PART>(a, b - qblocks);
   }
-  if (late) grid_launch_dependents();
 }
 
 }  // namespace
@@ -60,7 +55,7 @@ bool route_uses_warp_body(int E, const float* logits, const float* bias, const f
 int route_quantize(const float* logits, const float* bias, int T, int E, int K, int renormalize, float scale,
                    int32_t* ids, float* weights, uint16_t* weights_bf16, const uint16_t* latent, int rows, int cols,
                    uint8_t* q, uint8_t* scales, bool latent_ready, cudaStream_t s, const float* part, int S,
-                   uint32_t* smap, uint8_t* below, bool late_trigger) {
+                   uint32_t* smap, uint8_t* below) {
   using namespace moe::topk_impl;
   if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARGUMENT;
   if (E > MOE_MAX_EXPERTS || K > MOE_MAX_TOPK) return MOE_ERR_CAPACITY;
@@ -92,12 +87,12 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   a.smap = smap;
   a.below = below;
   const dim3 grid((unsigned)(rblocks + qblocks)), block(kThreads);
-  const int qb = (int)qblocks, rb = (int)rblocks, qw = latent_ready ? 0 : 1, lt = late_trigger ? 1 : 0;
+  const int qb = (int)qblocks, rb = (int)rblocks, qw = latent_ready ? 0 : 1;
 #define MOE_RQ_LAUNCH(NJ, W)                                                                                      \
   return part ? launch_pdl(route_quant_kernel<NJ, W, true>, grid, block, 0, s, a, latent, nchunks, q, scales,     \
-                           dev.error_word, qb, rb, qw, lt)                                                            \
+                           dev.error_word, qb, rb, qw)                                                            \
               : launch_pdl(route_quant_kernel<NJ, W, false>, grid, block, 0, s, a, latent, nchunks, q, scales,    \
-                           dev.error_word, qb, rb, qw, lt);
+                           dev.error_word, qb, rb, qw);
   if (E > kWarpMaxE) {
     MOE_RQ_LAUNCH(32, false)
   }

@@ -14,6 +14,17 @@ int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int 
 constexpr int kGemvMaxTokens = 8;
 int launch_router_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, cudaStream_t stream);
 
+// The one-call step's MXFP8 of the latent (mxfp8_quantize_rows, OCP floor rule,
+// row-major scales), done by the tensor-core router's epilogue warps while its mainloop
+// runs: the flat input of nchunks 16-byte chunks (16-byte aligned), q (8-byte aligned),
+// scales (8-byte aligned).
+struct LatentQuant {
+  const uint16_t* x = nullptr;
+  long long nchunks = 0;
+  uint8_t* q = nullptr;
+  uint8_t* scales = nullptr;
+};
+
 // Tensor-core (tcgen05) split-K path.
 struct TcPlan {
   int bn;    // token tile: 16, 32, 64, 128 or 256
@@ -35,7 +46,7 @@ inline size_t tc_workspace(const TcPlan& p, int T, int E) {
 TcPlan tc_plan(int T, int H, int E, int sm_count);         // single CTAs or CTA pairs
 TcPlan tc_plan_single(int T, int H, int E, int sm_count);  // single CTAs only
 int launch_router_tc(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, const TcPlan& p,
-                     float* part, uint32_t* err, cudaStream_t stream);
+                     float* part, uint32_t* err, cudaStream_t stream, const LatentQuant* lq = nullptr);
 
 // The front projection: router logits (FP32 [T, E]) and the latent down projection
 // (BF16 [T, L], one rounding of the FP32 sum) in one tensor-core launch over x. The
@@ -47,8 +58,11 @@ int launch_front_tc(const uint16_t* x, const uint16_t* w, const uint16_t* w2, fl
 
 // The tensor-core router's split-K partials [S][T][E] without their reduction (the
 // consumer sums them in split order; S == 1: logits written directly). *S_out = S.
+// With lq, the launch also quantises the latent when it runs the tensor-core kernel
+// (*quantised = true; false for the few-token GEMV, which leaves it to the caller).
 int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int sm_count,
-                           float* part, uint32_t* err, cudaStream_t stream, int* S_out);
+                           float* part, uint32_t* err, cudaStream_t stream, int* S_out,
+                           const LatentQuant* lq = nullptr, bool* quantised = nullptr);
 size_t router_partials_bytes(int T, int H, int E, int sm_count);
 
 // logits = sum over s of part[s] (split order), part [S][T][E].

@@ -333,9 +333,9 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
     b4[j] = (a.bias && e < E) ? __ldg(reinterpret_cast<const float4*>(a.bias + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (e < E) *reinterpret_cast<float4*>(&ws.x[e]) = x4[j];  // the row, for the candidates' exact keys
   }
-  // 1) approximate keys as floats (NaN never a candidate); the lane maximum
-  float c[NJ];
-  float m = -INFINITY;
+  // 1) approximate keys as floats (NaN never a candidate); the lane maximum, as a tree
+  //    (fmaxf ignores NaN; all NaN gives NaN, taken as -inf below)
+  float c[NJ], mx[NJ];
 #pragma unroll
   for (int j = 0; j < NJ4; ++j) {
     const float xs[4] = {x4[j].x, x4[j].y, x4[j].z, x4[j].w}, bs[4] = {b4[j].x, b4[j].y, b4[j].z, b4[j].w};
@@ -343,9 +343,16 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
     for (int i = 0; i < 4; ++i) {
       const float sv = approx_sigmoid(xs[i]);
       c[4 * j + i] = 128 * j + 4 * lane < E ? (a.bias ? __fadd_rn(sv, bs[i]) : sv) : -INFINITY;
-      m = fmaxf(m, c[4 * j + i]);  // (ignores NaN)
+      mx[4 * j + i] = c[4 * j + i];
     }
   }
+#pragma unroll
+  for (int w = NJ; w > 1; w = (w + 1) / 2) {
+#pragma unroll
+    for (int i = 0; i < w / 2; ++i) mx[i] = fmaxf(mx[2 * i], mx[2 * i + 1]);
+    if (w & 1) mx[w / 2] = mx[w - 1];
+  }
+  const float m = mx[0];
   // 2) bound: the K-th largest of the 32 lane maxima, sorted descending over shuffles
   //    (-inf for a lane without a number)
   float v = m != m ? -INFINITY : m;
@@ -377,9 +384,9 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
   const int total = __shfl_sync(kFull, incl, 31);
   if (isfinite(thr) && total >= K && total <= 64) {
     int pos = incl - mine;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (flags & (1u << j)) ws.e[pos++] = 128 * (j >> 2) + 4 * lane + (j & 3);
+    for (uint32_t f = flags; f != 0u; f &= f - 1u) {  // (a lane's few candidates, ascending)
+      const int j = __ffs(f) - 1;
+      ws.e[pos++] = 128 * (j >> 2) + 4 * lane + (j & 3);
     }
     __syncwarp();
     // 4) exact keys of the candidates (lane i: candidates i and i + 32); a candidate's
@@ -396,9 +403,9 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
       c1 = rank_key(exact_key(a, ws.x[e], a.bias ? __ldg(a.bias + e) : 0.f, &s1), e);
     }
     int r0 = 0, r1 = 0;
-    if (total <= 32) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) r0 += __shfl_sync(kFull, c0, i) > c0;
+    if (total <= 32) {  // (lanes past `total` hold no candidate: key 0, ordering below all)
+#pragma unroll 4
+      for (int i = 0; i < total; ++i) r0 += __shfl_sync(kFull, c0, i) > c0;
     } else {
 #pragma unroll 8
       for (int i = 0; i < 32; ++i) {
@@ -615,12 +622,11 @@ __device__ __forceinline__ void topk_token_cta(const TopkArgs& a, const int t) {
 // The routing part of a launch: CTA `blk` of the routing CTAs. Warp body (NJ = experts
 // per lane / 4): its 4 warps take tokens 4 blk .. 4 blk + 3; CTA body (NJ = experts
 // per thread): token blk. Waits for the preceding kernel (which writes the logits or
-// partials) before reading. trigger: let the dependent grid launch at the start (else
-// the caller does, later).
+// partials) before reading.
 template <int NJ, bool WARP, bool PART>
-__device__ __forceinline__ void route_block(const TopkArgs& a, int blk, bool trigger = true) {
+__device__ __forceinline__ void route_block(const TopkArgs& a, int blk) {
   __shared__ uint32_t s_map[WARP ? kWarpMaxE : 1];
-  if (trigger) grid_launch_dependents();
+  grid_launch_dependents();
   if (!PART && (a.E & 3) == 0) {
     // the logits rows' DRAM fetch overlaps the preceding kernel's end (a hint only)
     const int t = WARP ? blk * kWarps + (int)(threadIdx.x >> 5) : blk;
@@ -644,9 +650,12 @@ __device__ __forceinline__ void route_block(const TopkArgs& a, int blk, bool tri
       if (warp == 0) {
         // this block's pairs below each range (nr <= 32 here: E <= kWarpMaxE): a scan of
         // the per-range counts (slot bytes are below 0x80, absent ones 0xFF)
+        // (lane l reads word 32 i + l of range i: conflict-free; a warp sum per range)
         int c = 0;
-        if (lane < nr)
-          for (int e = 32 * lane; e < 32 * lane + 32; ++e) c += __popc(~s_map[e] & 0x80808080u);
+        for (int i = 0; i < nr; ++i) {
+          const int v = __reduce_add_sync(kFull, __popc(~s_map[32 * i + lane] & 0x80808080u));
+          if (lane == i) c = v;
+        }
         int inc = c;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
