@@ -15,23 +15,77 @@
 // exponent field. v * 2^-se is one exact FP32 multiply (or underflows far below half
 // the smallest E4M3 subnormal); cvt.rn.satfinite.e4m3x2.f32 rounds two at a time. A
 // warp writes its 8 elements' bytes per lane (256 contiguous bytes) and its 8 scale
-// bytes as one 8-byte store. The input is one contiguous span: each CTA stages its
-// 16 KB piece with a single bulk (TMA) copy onto an mbarrier, so every CTA's whole
-// input is in flight at once; threads then read their chunks from shared memory
-// (consecutive lanes, consecutive 16 bytes: conflict-free).
+// bytes as one 8-byte store. The input is one contiguous span: one CTA per SM takes a
+// contiguous run of 16 KB stages and keeps four bulk (TMA) copies in flight on
+// mbarriers; threads read their chunks from shared memory (consecutive lanes,
+// consecutive 16 bytes: conflict-free). (One 16 KB CTA per stage instead left a few
+// SMs with more of a call's CTAs than others -- back-to-back calls place them while
+// earlier calls' still run -- and measured 5.9-6.1 us a call at T = 1020.)
 #include "mxfp8.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kThreads = 512;
+constexpr int kStageChunks = 1024;  // 16 KB of input per stage (a multiple of 32 chunks)
+constexpr int kStages = 4;          // 64 KB of stages per CTA
 
+// One CTA per SM (at most): CTA b takes a contiguous run of whole stages of the input,
+// keeps up to kStages bulk copies of it in flight on mbarriers, converts each stage as
+// it lands (512 threads, two warp groups of 32 chunks per warp) and refills the buffer.
+// Before its wait the CTA asks L2 for its whole run (a hint), so the DRAM fetch
+// overlaps the preceding kernel's end.
 template <bool CEIL, bool TILED>
 __global__ void __launch_bounds__(kThreads) mxfp8_kernel(const uint16_t* __restrict__ x, long long nchunks,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ scales,
                                                          uint32_t* err, int rows, int nsc, int ct) {
-  mxfp8_impl::mxfp8_block<kThreads, kUnroll, CEIL, TILED>(x, nchunks, q, scales, err, blockIdx.x, true, nsc, ct);
+  extern __shared__ __align__(128) uint4 stage[];  // [kStages][kStageChunks]
+  __shared__ __align__(8) uint64_t bar_mem[kStages];
+  const int lane = threadIdx.x & 31;
+  const long long nst = (nchunks + kStageChunks - 1) / kStageChunks;
+  const long long s0 = (long long)blockIdx.x * nst / gridDim.x, s1 = ((long long)blockIdx.x + 1) * nst / gridDim.x;
+  const int n = (int)(s1 - s0);  // this CTA's stages
+  auto bar = [&](int b) { return smem_u32(&bar_mem[b]); };
+  auto span = [&](int i) { return (int)min((long long)kStageChunks, nchunks - (s0 + i) * kStageChunks); };
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kStages; ++b) mbar_init(bar(b), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();  // the barriers are initialised before any thread waits on them
+  grid_launch_dependents();
+  if (threadIdx.x == 0 && n > 0)  // (its first kStages stages)
+    prefetch_l2(x + s0 * kStageChunks * 8,
+                (uint32_t)((min(min(s1, s0 + kStages) * kStageChunks, nchunks) - s0 * kStageChunks) * 16));
+  grid_wait();
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int i) {
+    const int b = i % kStages;
+    mbar_expect_tx(bar(b), (uint32_t)span(i) * 16u);
+    bulk_g2s(smem_u32(stage + (size_t)b * kStageChunks), x + (s0 + i) * kStageChunks * 8, (uint32_t)span(i) * 16u,
+             bar(b), pol);
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < n && i < kStages; ++i) issue(i);
+  for (int i = 0; i < n; ++i) {
+    const int b = i % kStages;
+    if (!__syncthreads_and(mbar_wait(bar(b), (uint32_t)(i / kStages) & 1u, err))) {
+      // (a stage never landed: error set; the copies still in flight are waited for,
+      // each with the same bound, before the CTA leaves)
+      for (int j = i + 1; j < n && j < i + kStages; ++j) mbar_wait(bar(j % kStages), (uint32_t)(j / kStages) & 1u, err);
+      break;
+    }
+    const long long c0 = (s0 + i) * kStageChunks;
+    const int nch = span(i);
+#pragma unroll
+    for (int u = 0; u < kStageChunks / kThreads; ++u) {
+      const int wl = u * kThreads + (threadIdx.x & ~31);  // this warp's first chunk in the stage
+      if (wl >= nch) break;                                // warp-uniform
+      const uint4 v = wl + lane < nch ? stage[(size_t)b * kStageChunks + wl + lane] : make_uint4(0, 0, 0, 0);
+      mxfp8_impl::convert_warp<CEIL, TILED>(v, c0 + wl, nchunks, q, scales, nsc, ct);
+    }
+    __syncthreads();  // every thread is done with buffer b
+    if (threadIdx.x == 0 && i + kStages < n) issue(i + kStages);
+  }
   if (TILED) mxfp8_impl::tcgen05_scale_padding(scales, rows, nsc, ct);
 }
 
@@ -46,14 +100,16 @@ int quantize(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   const long long nchunks = (long long)rows * (cols / 8);
-  const long long per = (long long)kThreads * kUnroll;
-  const long long blocks = (nchunks + per - 1) / per;
-  if (blocks > (1LL << 31) - 1) return MOE_ERR_CAPACITY;
+  const long long nst = (nchunks + kStageChunks - 1) / kStageChunks;
+  const long long blocks = nst < dev.sm_count ? nst : dev.sm_count;
   const int nsc = cols / 32, ct = (nsc + 3) / 4;
   const bool ceil = scale_rule == MXFP8_SCALE_CEIL;
   auto kern = tiled ? (ceil ? mxfp8_kernel<true, true> : mxfp8_kernel<false, true>)
                     : (ceil ? mxfp8_kernel<true, false> : mxfp8_kernel<false, false>);
-  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, stream, x, nchunks, q, scales, dev.error_word,
+  constexpr size_t smem = (size_t)kStages * kStageChunks * 16;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), smem, stream, x, nchunks, q, scales, dev.error_word,
                     rows, nsc, ct);
 }
 
