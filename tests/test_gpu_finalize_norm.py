@@ -43,9 +43,11 @@ def test_decode_shapes(moe, orc, T):
 
 @pytest.mark.parametrize("T,K,H,wdt,eps", [(37, 16, 3584, "f32", 1e-5), (5, 3, 256, "bf16", 0.0),
                                            (9, 32, 1024, "f32", 1e-6), (4, 8, 8192, "bf16", 1e-5),
-                                           (3, 16, 7168, "bf16", 1e-5)])
+                                           (3, 16, 7168, "bf16", 1e-5), (400, 12, 3584, "bf16", 1e-5)])
 def test_shapes_and_chunks(moe, orc, T, K, H, wdt, eps):
-    """Ragged T, other K and widths; H = 7168 and 8192 take the rows in chunks."""
+    """Ragged T, other K and widths; H = 7168 and 8192 take the rows in chunks, and so
+    does a batch of more tokens than two CTAs per SM hold at once (three CTAs per SM,
+    chunks of ten rows)."""
     rows = synth.normal_bf16(21 + H, 4, (T * K, H))
     w = synth.normal_bf16(21, 7, (T, K), 0.25) if wdt == "bf16" else synth.normal_f32(21, 7, (T, K), 0.25)
     g = synth.norm_weight(l=H)
