@@ -14,6 +14,8 @@ namespace moe {
 struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
+  int smem_per_sm = 0;        // shared memory an SM holds (bytes)
+  int smem_reserved = 0;      // shared memory the system reserves per CTA (bytes)
   uint32_t* error_word = nullptr;  // device address of the library's error word
 };
 

@@ -15,12 +15,13 @@
 // exponent field. v * 2^-se is one exact FP32 multiply (or underflows far below half
 // the smallest E4M3 subnormal); cvt.rn.satfinite.e4m3x2.f32 rounds two at a time. A
 // warp writes its 8 elements' bytes per lane (256 contiguous bytes) and its 8 scale
-// bytes as one 8-byte store. The input is one contiguous span: one CTA per SM takes a
-// contiguous run of 16 KB stages and keeps four bulk (TMA) copies in flight on
-// mbarriers; threads read their chunks from shared memory (consecutive lanes,
-// consecutive 16 bytes: conflict-free). (One 16 KB CTA per stage instead left a few
-// SMs with more of a call's CTAs than others -- back-to-back calls place them while
-// earlier calls' still run -- and measured 5.9-6.1 us a call at T = 1020.)
+// bytes as one 8-byte store. The input is one contiguous span: CTAs of 512 threads
+// (up to three per SM) take contiguous runs of 16 KB stages and keep four bulk (TMA)
+// copies in flight on mbarriers; threads read their chunks from shared memory
+// (consecutive lanes, consecutive 16 bytes: conflict-free). (Small CTAs of one 16 KB
+// span each left a few SMs with more of a call's CTAs than others -- back-to-back calls
+// place them while earlier calls' still run -- and measured 5.9-6.1 us a call at
+// T = 1020; the 64 KB of stages per CTA caps every SM at three.)
 #include "mxfp8.cuh"
 
 namespace moe {
@@ -30,9 +31,11 @@ constexpr int kThreads = 512;
 constexpr int kStageChunks = 1024;  // 16 KB of input per stage (a multiple of 32 chunks)
 constexpr int kStages = 4;          // 64 KB of stages per CTA
 
-// One CTA per SM (at most): CTA b takes a contiguous run of whole stages of the input,
-// keeps up to kStages bulk copies of it in flight on mbarriers, converts each stage as
-// it lands (512 threads, two warp groups of 32 chunks per warp) and refills the buffer.
+// Up to three CTAs per SM (their stages' shared memory admits no more): CTA b takes a
+// contiguous run of whole stages of the input, keeps up to kStages bulk copies of it in
+// flight on mbarriers, converts each stage as it lands (512 threads, two warp groups of
+// 32 chunks per warp) and refills the buffer. (Measured back to back: one CTA per SM
+// 5.0 us a call at T = 1020 and 14.4 at 4096, two 6.5 / 12.0, three 4.1 / 11.4.)
 // Before its wait the CTA asks L2 for its whole run (a hint), so the DRAM fetch
 // overlaps the preceding kernel's end.
 template <bool CEIL, bool TILED>
@@ -101,7 +104,7 @@ int quantize(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* scales,
   if (st != MOE_OK) return st;
   const long long nchunks = (long long)rows * (cols / 8);
   const long long nst = (nchunks + kStageChunks - 1) / kStageChunks;
-  const long long blocks = nst < dev.sm_count ? nst : dev.sm_count;
+  const long long blocks = nst < 3LL * dev.sm_count ? nst : 3LL * dev.sm_count;
   const int nsc = cols / 32, ct = (nsc + 3) / 4;
   const bool ceil = scale_rule == MXFP8_SCALE_CEIL;
   auto kern = tiled ? (ceil ? mxfp8_kernel<true, true> : mxfp8_kernel<false, true>)
