@@ -310,7 +310,11 @@ int launch_one(FinArgs a, int sm_count, cudaStream_t s) {
     if (a.map_chunk < 1) return MOE_ERR_CAPACITY;
   }
   auto kern = finalize_kernel<KT, G, B, S, LISTS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
+  // (the limit is the instantiation's largest need, the same for every call: calls from
+  // several host threads never lower it under one another)
+  constexpr size_t most = (size_t)kStages * ((KT ? KT : MOE_MAX_TOPK) + (S ? 1 : 0)) * kThreads * 16;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) != cudaSuccess)
+    return MOE_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
     return MOE_ERR_CUDA;

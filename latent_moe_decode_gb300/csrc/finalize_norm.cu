@@ -160,7 +160,9 @@ template <bool G, bool B>
 int launch(const NormArgs& a, cudaStream_t s) {
   auto kern = finalize_norm_kernel<G, B>;
   const size_t smem = (size_t)a.KC * (a.H / 8) * 16;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  // (the limit is the largest staging any call uses, the same for every call: calls from
+  // several host threads never lower it under one another)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSlotBytes2) != cudaSuccess)
     return MOE_ERR_CUDA;
   return launch_pdl(kern, dim3((unsigned)a.T), dim3((unsigned)(a.H / 8)), smem, s, a);
 }

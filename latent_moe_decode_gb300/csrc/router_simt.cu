@@ -201,7 +201,11 @@ void simt_plan(int T, int H, int E, int sm_count, int* S, int* kc) {
 int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, int S, int kc,
                        float* part, cudaStream_t stream) {
   const size_t smem = (size_t)16 * kc * 2;
-  if (cudaFuncSetAttribute(router_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  // (the limit is the largest staging any plan uses -- kc <= 4096 -- the same for every
+  // call: calls from several host threads never lower it under one another)
+  if (kc > 4096) return MOE_ERR_INVALID_ARGUMENT;
+  if (cudaFuncSetAttribute(router_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16 * 4096 * 2) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   dim3 grid((E + 15) / 16, (T + 15) / 16, S);
   int st = launch_pdl(router_simt_kernel, grid, dim3(kThreads), smem, stream, x, w, S == 1 ? logits : part, T, H, E, kc);

@@ -59,12 +59,16 @@ size_t cta_cap_pad(const void* kern, long long blocks, const DeviceInfo& dev) {
   return pad > 0 ? (size_t)pad : 0;
 }
 
+// The kernel's dynamic shared memory limit is always set to the largest pad (the cap of
+// two), never lowered, so that calls from several host threads with different pads
+// cannot race on it.
 template <typename Kern>
 int launch_capped(Kern kern, dim3 grid, dim3 block, cudaStream_t s, const TopkArgs& a, const DeviceInfo& dev) {
-  const size_t pad = cta_cap_pad(reinterpret_cast<const void*>(kern), grid.x, dev);
-  if (pad > 0 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pad) != cudaSuccess)
+  const void* k = reinterpret_cast<const void*>(kern);
+  const size_t pad = cta_cap_pad(k, grid.x, dev), most = cta_cap_pad(k, 2LL * dev.sm_count, dev);
+  if (most > 0 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return launch_pdl(kern, grid, block, pad, s, a);
+  return launch_pdl(kern, grid, block, pad <= most ? pad : 0, s, a);
 }
 
 }  // namespace
