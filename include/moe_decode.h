@@ -104,7 +104,7 @@ int moe_router_logits(const uint16_t* x, const uint16_t* w, float* logits, int T
                       void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* The same computation with an explicit kernel family: MOE_ROUTER_AUTO (what
- * moe_router_logits uses: the CUDA cores for T <= 8, the tensor cores above),
+ * moe_router_logits uses: the CUDA cores for T <= 4, the tensor cores above),
  * MOE_ROUTER_SIMT (CUDA cores: the GEMV form for T <= 8, else split-K with per-lane
  * FP32 chains of at most 128 products and a fixed butterfly) or MOE_ROUTER_TCGEN05
  * (tensor-core split-K with a TMEM accumulator). The workspace query covers every
@@ -390,7 +390,7 @@ int moe_finalize_rmsnorm(const uint16_t* rows, int64_t n_rows, const int32_t* ro
  * expert) with the BF16 routing weights, as the wide page's Finalize does. Every
  * output equals the four calls' bit for bit. It takes three launches (programmatic
  * dependent launch between them): the router, whose warps that wait for its tensor-core
- * mainloop meanwhile quantise the latent to MXFP8 (for up to 8 tokens, whose router runs
+ * mainloop meanwhile quantise the latent to MXFP8 (for up to 4 tokens, whose router runs
  * on the CUDA cores, the next launch does); top-K, whose routing CTAs (four tokens each)
  * also write each token's slots by expert to the workspace; and Finalize, whose launch
  * also builds the routing lists from those slots

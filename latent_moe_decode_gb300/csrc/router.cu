@@ -10,7 +10,7 @@ constexpr int kAlgoAuto = 0, kAlgoSimt = 1, kAlgoTc = 2;
 // otherwise the tensor cores.
 int pick(int algo, int T) {
   if (algo != kAlgoAuto) return algo;
-  return T <= kGemvMaxTokens ? kAlgoSimt : kAlgoTc;
+  return T <= kAutoGemvMaxTokens ? kAlgoSimt : kAlgoTc;
 }
 
 size_t workspace_for(int T, int H, int E, int sm_count) {

@@ -59,7 +59,7 @@ extern "C" int moe_router_logits_noalloc(const uint16_t* x, const uint16_t* w, f
   int st = current_device(&dev);
   if (st != MOE_OK) return st;
   // the kernel moe_router_logits picks for a handful of tokens needs no scratch
-  if (T <= kGemvMaxTokens) return launch_router_gemv(x, w, logits, T, H, E, as_cuda(stream));
+  if (T <= kAutoGemvMaxTokens) return launch_router_gemv(x, w, logits, T, H, E, as_cuda(stream));
   const TcPlan p = tc_plan(T, H, E, dev.sm_count);
   const size_t need = tc_workspace(p, T, E);
   if (need > kScratchBytes) return MOE_ERR_CAPACITY;

@@ -773,7 +773,7 @@ int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, 
                            float* part, uint32_t* err, cudaStream_t stream, int* S_out, const LatentQuant* lq,
                            bool* quantised) {
   if (quantised) *quantised = false;
-  if (T <= kGemvMaxTokens) {  // what moe_router_logits runs for a handful of tokens
+  if (T <= kAutoGemvMaxTokens) {  // what moe_router_logits runs for a handful of tokens
     *S_out = 1;
     return launch_router_gemv(x, w, logits, T, H, E, stream);
   }
@@ -811,7 +811,7 @@ int launch_router_partials(const uint16_t* x, const uint16_t* w, float* logits, 
 }
 
 size_t router_partials_bytes(int T, int H, int E, int sm_count) {
-  if (T <= kGemvMaxTokens) return 0;
+  if (T <= kAutoGemvMaxTokens) return 0;
   const TcPlan p = tc_plan(T, H, E, sm_count);
   return (p.S > 1 && p.bn > 64) ? (size_t)p.S * T * E * sizeof(float) : 0;
 }

@@ -76,7 +76,7 @@ def test_wide_in_cuda_graph(moe, orc):
     _check_chain(moe, orc, 1020, graph=True)
 
 
-@pytest.mark.parametrize("T", [1, 8, 64, 100, 256, 1020, 2048, 4096])
+@pytest.mark.parametrize("T", [1, 4, 5, 8, 64, 100, 256, 1020, 2048, 4096])
 def test_one_call_equals_four_calls(moe, T):
     """moe_route_finalize == the four calls it stands for, every output bit for bit --
     including the logits, which the one call's top-K launch sums from the router's
