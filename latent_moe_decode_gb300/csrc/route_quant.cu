@@ -88,11 +88,24 @@ int route_quantize(const float* logits, const float* bias, int T, int E, int K, 
   a.below = below;
   const dim3 grid((unsigned)(rblocks + qblocks)), block(kThreads);
   const int qb = (int)qblocks, rb = (int)rblocks, qw = latent_ready ? 0 : 1;
+  // With partials and no more CTAs than SMs, an SM may hold at most two of them (unused
+  // dynamic shared memory): placed as the router's CTAs leave, they otherwise gathered
+  // on the SMs freed first (measured, the one-call step at T = 256: 22.9 against 23.5 us;
+  // at T = 1020, 255 CTAs, the cap measured 0.3 us slower and is not taken). The limit
+  // is that pad for every call, so that calls from several threads do not race on it.
+  const bool capped = part && grid.x <= (unsigned)dev.sm_count;
 #define MOE_RQ_LAUNCH(NJ, W)                                                                                      \
-  return part ? launch_pdl(route_quant_kernel<NJ, W, true>, grid, block, 0, s, a, latent, nchunks, q, scales,     \
-                           dev.error_word, qb, rb, qw)                                                            \
-              : launch_pdl(route_quant_kernel<NJ, W, false>, grid, block, 0, s, a, latent, nchunks, q, scales,    \
-                           dev.error_word, qb, rb, qw);
+  if (part) {                                                                                                     \
+    auto kern = route_quant_kernel<NJ, W, true>;                                                                  \
+    const size_t most = cta_cap_pad(reinterpret_cast<const void*>(kern), dev.sm_count, dev);                      \
+    if (most > 0 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) !=        \
+                        cudaSuccess)                                                                              \
+      return MOE_ERR_CUDA;                                                                                        \
+    return launch_pdl(kern, grid, block, capped ? most : 0, s, a, latent, nchunks, q, scales, dev.error_word, qb, \
+                      rb, qw);                                                                                    \
+  }                                                                                                               \
+  return launch_pdl(route_quant_kernel<NJ, W, false>, grid, block, 0, s, a, latent, nchunks, q, scales,           \
+                    dev.error_word, qb, rb, qw);
   if (E > kWarpMaxE) {
     MOE_RQ_LAUNCH(32, false)
   }

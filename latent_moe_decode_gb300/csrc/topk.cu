@@ -37,28 +37,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   route_block<NJ, WARP, false>(a, blockIdx.x);
 }
 
-// Dynamic shared memory (never touched) that lets an SM hold no more than the fewest
-// CTAs per SM one wave of `blocks` CTAs needs: back-to-back calls place a call's CTAs
-// while earlier calls' still hold the SMs, and uncapped some SMs took up to seven of
-// one call's CTAs, which then set its time (T = 1020: 5.9 us a call uncapped, 4.2
-// capped at two per SM; a cap below one wave's need measured slower, 13.5 us at T =
-// 4096 with two). 0 when no cap is needed.
-size_t cta_cap_pad(const void* kern, long long blocks, const DeviceInfo& dev) {
-  long long cap = (blocks + dev.sm_count - 1) / dev.sm_count;
-  if (cap < 2) cap = 2;  // (room for the next call's CTA beside this one's)
-  cudaFuncAttributes fa;
-  if (cap < 1 || dev.smem_per_sm <= 0 || cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  const long long fixed = (long long)fa.sharedSizeBytes + dev.smem_reserved;  // per CTA
-  const long long natural = dev.smem_per_sm / (fixed > 0 ? fixed : 1);     // (by shared memory alone)
-  if (cap >= natural || cap >= 8) return 0;
-  long long pad = dev.smem_per_sm / cap - fixed;
-  pad = pad / 1024 * 1024 - 1024;  // (round down, and a margin below the cap's limit)
-  return pad > 0 ? (size_t)pad : 0;
-}
-
 // The kernel's dynamic shared memory limit is always set to the largest pad (the cap of
 // two), never lowered, so that calls from several host threads with different pads
 // cannot race on it.
