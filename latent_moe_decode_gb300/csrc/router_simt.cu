@@ -89,14 +89,19 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
 // read before the wait for the preceding kernel only as a prefetch) so the stream
 // starts while the preceding kernel finishes.
 constexpr int kGemvWarps = 7;
-// expert rows per CTA: 2 (448 CTAs at E = 896, three resident per SM); 6 at 8 tokens
-// (150 CTAs, one per SM): the tokens' rows are re-read from L2 by every CTA, so fewer,
-// wider CTAs read them fewer times
+// Expert rows per CTA and CTAs per SM, by the rounded token count (measured back to back
+// over cold inputs at E = 896, H = 7168): 3 rows, two CTAs per SM, at 1 and 2 tokens
+// (3.6 / 4.1 us; 2 rows and three per SM: 4.0 / 4.7); 2 rows, three per SM, at 4 (5.3 us;
+// 3 rows: 6.0); 6 rows, one CTA per SM, at 8. The tokens' rows are re-read from L2 by
+// every CTA, so fewer, wider CTAs read them fewer times, until too few CTAs are resident
+// to keep the gate's stream in flight.
 template <int TT>
-constexpr int gemv_rows() { return TT == 8 ? 6 : 2; }
+constexpr int gemv_rows() { return TT == 8 ? 6 : (TT == 4 ? 2 : 3); }
+template <int TT>
+constexpr int gemv_ctas_per_sm() { return TT == 8 ? 1 : (TT == 4 ? 3 : 2); }
 
 template <int TT, int kGemvRows = gemv_rows<TT>()>
-__global__ void __launch_bounds__(kGemvWarps * 32, TT == 8 ? 1 : 3) router_gemv_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kGemvWarps * 32, gemv_ctas_per_sm<TT>()) router_gemv_kernel(const uint16_t* __restrict__ x,
                                                                       const uint16_t* __restrict__ w,
                                                                       float* __restrict__ out, int T, int H, int E) {
   __shared__ float red[kGemvWarps][kGemvRows * TT];
