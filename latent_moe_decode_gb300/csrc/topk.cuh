@@ -360,19 +360,22 @@ __device__ __forceinline__ void topk_token_warp(const TopkArgs& a, const int t, 
     if (w & 1) mx[w / 2] = mx[w - 1];
   }
   const float m = mx[0];
-  // 2) bound: the K-th largest of the 32 lane maxima, sorted descending over shuffles
-  //    (-inf for a lane without a number)
-  float v = m != m ? -INFINITY : m;
+  // 2) bound: the K-th largest of the 32 lane maxima (-inf for a lane without a number).
+  //    Each lane counts the maxima above its own and those at least its own (independent
+  //    shuffles, no chain of dependent exchanges); a lane with fewer than K above and at
+  //    least K at or above holds that value.
+  const float v = m != m ? -INFINITY : m;
+  int gt0 = 0, gt1 = 0, ge0 = 0, ge1 = 0;  // (two counters each: shorter add chains)
 #pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(kFull, v, j);
-      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-      v = keep_max ? fmaxf(v, o) : fminf(v, o);
-    }
+  for (int i = 0; i < 32; i += 2) {
+    const float o0 = __shfl_sync(kFull, v, i), o1 = __shfl_sync(kFull, v, i + 1);
+    gt0 += o0 > v;
+    ge0 += o0 >= v;
+    gt1 += o1 > v;
+    ge1 += o1 >= v;
   }
-  const float B = __shfl_sync(kFull, v, K - 1);
+  const unsigned holds = __ballot_sync(kFull, gt0 + gt1 < K && ge0 + ge1 >= K);
+  const float B = __shfl_sync(kFull, v, __ffs(holds) - 1);
   // every exact top-K expert has an approximate key within 2 err of the bound (err =
   // kApproxErr plus an ulp or two of the key); a bound that is not a finite number
   // sends the token to the all-exact path
