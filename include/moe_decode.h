@@ -93,7 +93,7 @@ int moe_device_error(uint32_t* bits, int clear);
  * Requirements: T >= 1, E >= 1, H >= 8, H % 8 == 0; x, w 16-byte aligned
  * (MOE_ERR_ALIGNMENT), logits 4-byte aligned.
  * Numerics: BF16 products are exact in FP32; sums are accumulated in FP32 -- for up
- * to 8 tokens on the CUDA cores (one pass over the gate, no split-K: per-lane chains
+ * to 4 tokens on the CUDA cores (one pass over the gate, no split-K: per-lane chains
  * of at most H / 224 fragments x 8 products, then fixed shuffle and warp trees), else
  * on the tensor cores in K-chunks with the split-K partials reduced in a fixed order
  * -- so the result is deterministic run to run. The error is well inside
