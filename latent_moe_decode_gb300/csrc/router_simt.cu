@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
   if (e < E && t < T) out[((size_t)s * T + t) * E + e] = acc[0];
 }
 
-// GEMV form for T <= 8 tokens (TT: the tokens rounded up to 1, 2, 4 or 8): the 12.8 MB
+// GEMV form for T <= 8 tokens (TT: the tokens rounded up to 1, 2, 3, 4 or 8): the 12.8 MB
 // gate is one HBM stream and the tokens' rows are small, so no K is split and no
 // partials leave the CTA. A CTA of kGemvWarps warps owns kGemvRows expert rows over the
 // whole hidden dimension; the 16-byte fragments f of a row are dealt to warps in runs
@@ -90,9 +90,9 @@ __global__ void __launch_bounds__(kThreads) router_simt_kernel(const uint16_t* _
 // starts while the preceding kernel finishes.
 constexpr int kGemvWarps = 7;
 // Expert rows per CTA and CTAs per SM, by the rounded token count (measured back to back
-// over cold inputs at E = 896, H = 7168): 3 rows, two CTAs per SM, at 1 and 2 tokens
-// (3.6 / 4.1 us; 2 rows and three per SM: 4.0 / 4.7); 2 rows, three per SM, at 4 (5.3 us;
-// 3 rows: 6.0); 6 rows, one CTA per SM, at 8. The tokens' rows are re-read from L2 by
+// over cold inputs at E = 896, H = 7168): 3 rows, two CTAs per SM, at 1, 2 and 3 tokens
+// (3.6 / 4.1 / 5.0 us; 2 rows and three per SM: 4.0 / 4.7 / 5.3-5.6); 2 rows, three per SM,
+// at 4 (5.3 us; 3 rows: 6.0); 6 rows, one CTA per SM, at 8. The tokens' rows are re-read from L2 by
 // every CTA, so fewer, wider CTAs read them fewer times, until too few CTAs are resident
 // to keep the gate's stream in flight.
 template <int TT>
@@ -227,6 +227,7 @@ int launch_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int 
 int launch_router_gemv(const uint16_t* x, const uint16_t* w, float* logits, int T, int H, int E, cudaStream_t stream) {
   if (T <= 1) return launch_gemv<1>(x, w, logits, T, H, E, stream);
   if (T <= 2) return launch_gemv<2>(x, w, logits, T, H, E, stream);
+  if (T <= 3) return launch_gemv<3>(x, w, logits, T, H, E, stream);
   if (T <= 4) return launch_gemv<4>(x, w, logits, T, H, E, stream);
   if (T <= kGemvMaxTokens) return launch_gemv<8>(x, w, logits, T, H, E, stream);
   return MOE_ERR_INVALID_ARGUMENT;
