@@ -13,7 +13,7 @@ int launch_router_simt(const uint16_t* x, const uint16_t* w, float* logits, int 
 // CUDA-core GEMV for T <= kGemvMaxTokens: no split-K, no workspace, one launch.
 constexpr int kGemvMaxTokens = 8;
 // The automatic choice (moe_router_logits, the one-call step) runs the GEMV only up to
-// this many tokens: its token count is rounded up to 1, 2, 4 or 8, and from 5 tokens the
+// this many tokens: its token count is rounded up to 1, 2, 3, 4 or 8, and from 5 tokens the
 // tcgen05 plan of one 16-token tile is faster (measured back to back over cold inputs:
 // 5.7 against 6.9 us at T = 4, 7.6 against 6.8 at T = 6, 7.8 against 6.8 at T = 8).
 constexpr int kAutoGemvMaxTokens = 4;
